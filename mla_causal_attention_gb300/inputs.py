@@ -1,0 +1,95 @@
+"""Seeded synthetic inputs for the MLA causal-attention core.
+
+This module holds no arithmetic of the attention method: it only draws random tensors of
+the shapes the attention core takes.  The same bf16 bit patterns feed both the CUDA
+library and the CPU oracle used by the tests.
+
+Recipe.  Every tensor is cut into chunks (one (b, h) slice of a per-head tensor, one b
+slice of the shared rotary key); each chunk has its own torch CPU generator seeded from
+(seed, tensor id, b, h) by a fixed integer mix, draws float32 N(0,1) values, is multiplied
+by the workload's scale factor and is rounded to bf16.  Chunking lets several threads
+draw at once and lets a test regenerate one batch row alone.  kv_len comes from its own
+generator (integers uniform in [lo, hi], inclusive).
+"""
+from __future__ import annotations
+
+import os
+from concurrent.futures import ThreadPoolExecutor
+
+import torch
+
+from .workloads import Workload
+
+_TENSOR_IDS = {"q_nope": 1, "q_pe": 2, "k_nope": 3, "k_pe_shared": 4, "v": 5, "kv_len": 6}
+_MASK64 = (1 << 64) - 1
+
+
+def chunk_seed(seed: int, tensor: str, b: int, h: int) -> int:
+    """A fixed 64-bit mix (splitmix64 finaliser) of the chunk's coordinates."""
+    x = (seed * 0x9E3779B97F4A7C15 + _TENSOR_IDS[tensor] * 0xBF58476D1CE4E5B9
+         + (b + 1) * 0x94D049BB133111EB + (h + 1) * 0x2545F4914F6CDD1D) & _MASK64
+    x ^= x >> 30
+    x = (x * 0xBF58476D1CE4E5B9) & _MASK64
+    x ^= x >> 27
+    x = (x * 0x94D049BB133111EB) & _MASK64
+    x ^= x >> 31
+    return x & ((1 << 63) - 1)
+
+
+def _draw(out: torch.Tensor, seed: int, tensor: str, b: int, h: int, factor: float) -> None:
+    g = torch.Generator("cpu").manual_seed(chunk_seed(seed, tensor, b, h))
+    x = torch.randn(out.shape, generator=g, dtype=torch.float32)
+    if factor != 1.0:
+        x.mul_(factor)
+    out.copy_(x.to(torch.bfloat16))
+
+
+def draw_kv_len(wl: Workload, seed: int) -> torch.Tensor:
+    if wl.kv_len_range is None:
+        return torch.full((wl.B,), wl.Tk, dtype=torch.int32)
+    lo, hi = wl.kv_len_range
+    g = torch.Generator("cpu").manual_seed(chunk_seed(seed, "kv_len", 0, 0))
+    return torch.randint(lo, hi + 1, (wl.B,), generator=g, dtype=torch.int64).to(torch.int32)
+
+
+def make_inputs(wl: Workload, seed: int = 0, pin_memory: bool = False,
+                threads: int | None = None, batches=None) -> dict:
+    """Host (CPU) bf16 inputs for a workload.
+
+    Returns a dict with q_nope [B,H,Tq,128], q_pe [B,H,Tq,64], k_nope [B,H,Tk,128],
+    k_pe_shared [B,Tk,64], v [B,H,Tk,128] (bf16), kv_len [B] (int32), past_len,
+    softmax_scale and the workload.  ``batches`` restricts generation to a subset of b
+    (the returned tensors then have len(batches) rows, drawn exactly as in the full set).
+    """
+    kv_len_full = draw_kv_len(wl, seed)
+    bs = list(range(wl.B)) if batches is None else [int(b) for b in batches]
+    nb = len(bs)
+    H, Tq, Tk = wl.H, wl.Tq, wl.Tk
+    alloc = dict(dtype=torch.bfloat16, pin_memory=pin_memory)
+    t = {
+        "q_nope": torch.empty((nb, H, Tq, 128), **alloc),
+        "q_pe": torch.empty((nb, H, Tq, 64), **alloc),
+        "k_nope": torch.empty((nb, H, Tk, 128), **alloc),
+        "k_pe_shared": torch.empty((nb, Tk, 64), **alloc),
+        "v": torch.empty((nb, H, Tk, 128), **alloc),
+    }
+    jobs = []
+    for bi, b in enumerate(bs):
+        for name in ("q_nope", "q_pe", "k_nope", "v"):
+            for h in range(H):
+                jobs.append((t[name][bi, h], name, b, h))
+        jobs.append((t["k_pe_shared"][bi], "k_pe_shared", b, 0))
+    n = threads or min(32, len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity")
+                       else (os.cpu_count() or 1))
+    f = wl.value_scale
+    if n <= 1 or len(jobs) < 4:
+        for out, name, b, h in jobs:
+            _draw(out, seed, name, b, h, f)
+    else:
+        with ThreadPoolExecutor(n) as ex:
+            list(ex.map(lambda j: _draw(j[0], seed, j[1], j[2], j[3], f), jobs))
+    kv_len = kv_len_full[bs].clone()
+    if pin_memory:
+        kv_len = kv_len.pin_memory()
+    t.update(kv_len=kv_len, past_len=wl.past_len, softmax_scale=wl.softmax_scale, workload=wl)
+    return t

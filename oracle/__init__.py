@@ -1,0 +1,6 @@
+"""fp64 CPU oracle of the Kimi K2 MLA causal-attention core.
+
+TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the CPU-baseline leg of the
+benchmark use it to check and time the CUDA library.  The library never imports it.
+"""
+from .oracle import build_oracle, oracle_rows, oracle_full, round_bf16, library_path  # noqa: F401

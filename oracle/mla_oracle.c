@@ -1,0 +1,239 @@
+/*
+ * mla_oracle.c -- plain fp64 CPU oracle for the Kimi K2 MLA causal-attention core.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the correctness reference that the CUDA
+ * library is checked against.  Only the test suite, the smoke check and the CPU
+ * baseline leg of the benchmark may load it.  The product path never calls it and
+ * shares no code, header or constant with it.
+ *
+ * What it computes, step by step, in the order of the attention excerpt on the page
+ * "Kimi K2 · Similarities" (section "Contextual evidence from Query-key similarity",
+ * the MLA forward of modeling_deepseek.py):
+ *
+ *   1. query row   Q = [q_nope | q_pe]                       (query concat)
+ *   2. key row     K = [k_nope | k_pe]   with k_pe the single rotary key of the
+ *                  sequence, broadcast to every head        (key concat; "the key's
+ *                  rotated part being the shared rotary key")
+ *   3. score       s_j = (Q . K_j) * softmax_scale          (matmul, then scale)
+ *   4. mask        s_j += M[i, j]                           (additive 4D mask)
+ *   5. weights     w_j = exp(s_j - max) / sum exp(s - max)  (softmax over keys)
+ *   6. output      o   = sum_j w_j V_j                      (weights times values)
+ *
+ * The cast of the weights to bf16 and dropout (p = attention_dropout = 0.0 in the
+ * config.json excerpt on "Kimi K2 · Logits") are not applied in the exact mode: the
+ * oracle is the exact value of the method, in fp64.
+ *
+ * Readings of points the pages leave open (each is listed in the design notes):
+ *   - The mask (built by _prepare_4d_causal_attention_mask on "Kimi K2 · Causal mask",
+ *     section "Construct causal mask"; its body is not shown) is 0 where key j is
+ *     visible to query i and the most negative finite bf16 value elsewhere.  Key j is
+ *     visible to query i iff j <= i + past_len (positions are numbered from the cached
+ *     length) and j < kv_len[b] (right padding).  A key masked for both reasons gets
+ *     the same single minimum, not twice it.
+ *   - Tk = past_len + Tq: the cache update puts the cached prefix first and the new
+ *     rows last.
+ *   - softmax_scale is an argument; it is used as the float it arrives as, widened to
+ *     double.
+ *
+ * Mode 1 ("eager") is a diagnostic: it rounds to bf16 where the eager PyTorch code on
+ * the page produces a bf16 tensor (matmul output, scaled scores, masked scores, the
+ * weights after the fp32 softmax, the output) and keeps everything else in fp64.  It
+ * shows how far the eager bf16 sequence sits from the exact value; it is not a gate.
+ *
+ * Build: gcc -O2 -ffp-contract=off -fPIC -shared -pthread (no fast-math).
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define D_NOPE 128 /* qk_nope_head_dim, config.json excerpt */
+#define D_ROPE 64  /* qk_rope_head_dim */
+#define D_V 128    /* v_head_dim */
+
+/* Exact widening of a bf16 bit pattern: bf16 is the top half of an IEEE fp32. */
+static double bf16_to_double(uint16_t bits) {
+  uint32_t u = ((uint32_t)bits) << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* Round a double to the nearest bf16 value (ties to even), returned as double.
+ * Used only by the eager-emulation diagnostic.  Goes through fp32 first, as the eager
+ * code computes in fp32 before it stores bf16; values are finite here. */
+static double round_bf16(double x) {
+  float f = (float)x;
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  if ((u & 0x7f800000u) == 0x7f800000u) return (double)f; /* inf / nan untouched */
+  uint32_t lsb = (u >> 16) & 1u;
+  u += 0x7fffu + lsb;
+  u &= 0xffff0000u;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* finfo(bfloat16).min = -(2 - 2^-7) * 2^127, the value the 4D mask holds where a key
+ * is hidden (the mask is built in the dtype of inputs_embeds, torch_dtype bfloat16). */
+static const double MASK_MIN_BF16 = -3.3895313892515355e38;
+
+typedef struct {
+  const uint16_t *q_nope, *q_pe, *k_nope, *k_pe, *v;
+  const int32_t* kv_len;
+  int64_t B, H, Tq, Tk, past_len;
+  double scale;
+  const int64_t* rows;
+  int64_t n_rows;
+  int mode;
+  double* out;
+  double* wsum;
+  int64_t next; /* shared work counter, guarded by lock */
+  pthread_mutex_t lock;
+  int err;
+} job_t;
+
+/* One output row o[b, h, i, :].  s is scratch of Tk doubles. */
+static int one_row(const job_t* J, int64_t flat, double* s, double* o, double* wsum_out) {
+  const int64_t i = flat % J->Tq;
+  const int64_t bh = flat / J->Tq;
+  const int64_t b = bh / J->H;
+  if (b >= J->B) return 1;
+  const int64_t kvl = J->kv_len ? (int64_t)J->kv_len[b] : J->Tk;
+  if (kvl < 1 || kvl > J->Tk) return 2;
+  const int eager = (J->mode == 1);
+
+  /* Step 1: query row Q = [q_nope | q_pe] (192 values). */
+  double q[D_NOPE + D_ROPE];
+  const uint16_t* qn = J->q_nope + (bh * J->Tq + i) * D_NOPE;
+  const uint16_t* qr = J->q_pe + (bh * J->Tq + i) * D_ROPE;
+  for (int d = 0; d < D_NOPE; ++d) q[d] = bf16_to_double(qn[d]);
+  for (int d = 0; d < D_ROPE; ++d) q[D_NOPE + d] = bf16_to_double(qr[d]);
+
+  /* The scale is a Python float multiplied into a bf16 tensor: eager computes the product
+   * with the scale as an fp32 value, which is what J->scale holds in both modes. */
+  const double scale_used = J->scale;
+  for (int64_t j = 0; j < J->Tk; ++j) {
+    /* Step 2: key row K_j = [k_nope[b,h,j] | k_pe[b,j]]; the rotary part has no head index. */
+    const uint16_t* kn = J->k_nope + (bh * J->Tk + j) * D_NOPE;
+    const uint16_t* kr = J->k_pe + (b * J->Tk + j) * D_ROPE;
+    /* Step 3: dot product over all 192 columns, then the scale. */
+    double acc = 0.0;
+    for (int d = 0; d < D_NOPE; ++d) acc += q[d] * bf16_to_double(kn[d]);
+    for (int d = 0; d < D_ROPE; ++d) acc += q[D_NOPE + d] * bf16_to_double(kr[d]);
+    if (eager) acc = round_bf16(acc);
+    double sj = acc * scale_used;
+    if (eager) sj = round_bf16(sj);
+    /* Step 4: additive mask. */
+    const int visible = (j <= i + J->past_len) && (j < kvl);
+    sj += visible ? 0.0 : MASK_MIN_BF16;
+    if (eager) sj = round_bf16(sj);
+    s[j] = sj;
+  }
+
+  /* Step 5: softmax over the key axis (max-subtracted, then normalised). */
+  double m = s[0];
+  for (int64_t j = 1; j < J->Tk; ++j)
+    if (s[j] > m) m = s[j];
+  double denom = 0.0;
+  for (int64_t j = 0; j < J->Tk; ++j) {
+    s[j] = exp(s[j] - m);
+    denom += s[j];
+  }
+  double wsum = 0.0;
+  for (int64_t j = 0; j < J->Tk; ++j) {
+    s[j] = s[j] / denom;
+    if (eager) s[j] = round_bf16(s[j]);
+    wsum += s[j];
+  }
+
+  /* Step 6: weighted sum of value rows. */
+  for (int d = 0; d < D_V; ++d) o[d] = 0.0;
+  for (int64_t j = 0; j < J->Tk; ++j) {
+    const double w = s[j];
+    if (w == 0.0) continue; /* adds exactly zero; skipping does not change the sum */
+    const uint16_t* vr = J->v + (bh * J->Tk + j) * D_V;
+    for (int d = 0; d < D_V; ++d) o[d] += w * bf16_to_double(vr[d]);
+  }
+  if (eager)
+    for (int d = 0; d < D_V; ++d) o[d] = round_bf16(o[d]);
+  if (wsum_out) *wsum_out = wsum;
+  return 0;
+}
+
+static void* worker(void* arg) {
+  job_t* J = (job_t*)arg;
+  double* s = (double*)malloc(sizeof(double) * (size_t)(J->Tk > 0 ? J->Tk : 1));
+  if (!s) {
+    pthread_mutex_lock(&J->lock);
+    J->err = 3;
+    pthread_mutex_unlock(&J->lock);
+    return NULL;
+  }
+  for (;;) {
+    pthread_mutex_lock(&J->lock);
+    int64_t r0 = J->next;
+    J->next += 16;
+    pthread_mutex_unlock(&J->lock);
+    if (r0 >= J->n_rows) break;
+    int64_t r1 = r0 + 16 < J->n_rows ? r0 + 16 : J->n_rows;
+    for (int64_t r = r0; r < r1; ++r) {
+      const int64_t flat = J->rows ? J->rows[r] : r;
+      int e = one_row(J, flat, s, J->out + r * D_V, J->wsum ? J->wsum + r : NULL);
+      if (e) {
+        pthread_mutex_lock(&J->lock);
+        J->err = e;
+        pthread_mutex_unlock(&J->lock);
+      }
+    }
+  }
+  free(s);
+  return NULL;
+}
+
+/*
+ * Compute output rows of the attention core.
+ *   q_nope [B,H,Tq,128], q_pe [B,H,Tq,64], k_nope [B,H,Tk,128], k_pe [B,Tk,64],
+ *   v [B,H,Tk,128]: bf16 bit patterns, row-major, contiguous.
+ *   kv_len [B] (int32, may be NULL meaning Tk for every sequence).
+ *   rows: n_rows flat row indices ((b*H + h)*Tq + i); NULL means all B*H*Tq rows.
+ *   out [n_rows,128] and wsum [n_rows] (may be NULL): written as double.
+ * Returns 0, or a nonzero code for bad arguments (shape, kv_len out of [1,Tk], alloc).
+ */
+int mla_oracle_rows(const uint16_t* q_nope, const uint16_t* q_pe, const uint16_t* k_nope,
+                    const uint16_t* k_pe, const uint16_t* v, const int32_t* kv_len, int64_t B,
+                    int64_t H, int64_t Tq, int64_t Tk, int64_t past_len, float softmax_scale,
+                    const int64_t* rows, int64_t n_rows, int mode, int nthreads, double* out,
+                    double* wsum) {
+  if (B < 1 || H < 1 || Tq < 1 || Tk < 1 || past_len < 0 || Tk != past_len + Tq) return 10;
+  if (!q_nope || !q_pe || !k_nope || !k_pe || !v || !out) return 11;
+  if (mode != 0 && mode != 1) return 12;
+  if (rows) {
+    for (int64_t r = 0; r < n_rows; ++r)
+      if (rows[r] < 0 || rows[r] >= B * H * Tq) return 13;
+  } else {
+    n_rows = B * H * Tq;
+  }
+  job_t J;
+  memset(&J, 0, sizeof J);
+  J.q_nope = q_nope; J.q_pe = q_pe; J.k_nope = k_nope; J.k_pe = k_pe; J.v = v;
+  J.kv_len = kv_len;
+  J.B = B; J.H = H; J.Tq = Tq; J.Tk = Tk; J.past_len = past_len;
+  J.scale = (double)softmax_scale;
+  J.rows = rows; J.n_rows = n_rows; J.mode = mode; J.out = out; J.wsum = wsum;
+  pthread_mutex_init(&J.lock, NULL);
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 256) nthreads = 256;
+  pthread_t th[256];
+  int started = 0;
+  for (int t = 0; t < nthreads; ++t)
+    if (pthread_create(&th[t], NULL, worker, &J) == 0) ++started;
+  if (started == 0) worker(&J);
+  for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
+  pthread_mutex_destroy(&J.lock);
+  return J.err;
+}
+
+/* Exposed for the test that pins the diagnostic rounding against torch's own cast. */
+double mla_oracle_round_bf16(double x) { return round_bf16(x); }

@@ -1,0 +1,135 @@
+"""ctypes front end of the fp64 CPU oracle (mla_oracle.c).
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product package imports this module.
+
+The oracle takes the same bf16 bit patterns the CUDA library takes (as numpy uint16
+arrays or CPU torch bfloat16 tensors) and returns exact fp64 output rows of the attention
+core described on the page "Kimi K2 · Similarities" (section "Contextual evidence from
+Query-key similarity"): scores over the concatenated 192-wide query/key, scale, additive
+causal/padding mask, softmax, weighted sum of the 128-wide values.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mla_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_BUILD, "libmla_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB
+
+
+def build_oracle(force: bool = False) -> str:
+    """Compile mla_oracle.c with gcc (IEEE arithmetic: no fast-math, no FMA contraction)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    stale = (not os.path.exists(_LIB)) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)
+    if force or stale:
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+               "-pthread", "-Wall", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            # MLA_ORACLE_LIB points the loader at another build of mla_oracle.c; the
+            # mutation test uses it to check that the pins fail on planted mistakes.
+            path = os.environ.get("MLA_ORACLE_LIB")
+            if not path:
+                path = build_oracle()
+            lib = ctypes.CDLL(path)
+            p = ctypes.c_void_p
+            i64 = ctypes.c_int64
+            lib.mla_oracle_rows.restype = ctypes.c_int
+            lib.mla_oracle_rows.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, i64,
+                                            ctypes.c_float, p, i64, ctypes.c_int, ctypes.c_int,
+                                            p, p]
+            lib.mla_oracle_round_bf16.restype = ctypes.c_double
+            lib.mla_oracle_round_bf16.argtypes = [ctypes.c_double]
+            _lib = lib
+    return _lib
+
+
+def _bits(x) -> np.ndarray:
+    """bf16 bit patterns as a C-contiguous uint16 numpy array (no copy where possible)."""
+    if isinstance(x, np.ndarray):
+        assert x.dtype == np.uint16
+        return np.ascontiguousarray(x)
+    import torch  # local: only tensors need it
+
+    assert x.dtype == torch.bfloat16 and x.device.type == "cpu"
+    return np.ascontiguousarray(x.contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+def _threads(n):
+    if n:
+        return int(n)
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def oracle_rows(q_nope, q_pe, k_nope, k_pe_shared, v, kv_len, past_len: int,
+                softmax_scale: float, rows=None, mode: str = "exact", threads: int | None = None,
+                return_wsum: bool = False):
+    """Exact fp64 output rows.
+
+    Shapes: q_nope [B,H,Tq,128], q_pe [B,H,Tq,64], k_nope [B,H,Tk,128],
+    k_pe_shared [B,Tk,64], v [B,H,Tk,128] (bf16), kv_len [B] int32 or None.
+    rows: flat indices (b*H + h)*Tq + i, or None for all rows in that order.
+    Returns float64 [n_rows,128] (and the per-row weight sum if asked).
+    """
+    lib = _load()
+    qn, qr, kn, kr, vv = (_bits(t) for t in (q_nope, q_pe, k_nope, k_pe_shared, v))
+    B, H, Tq, dn = qn.shape
+    Tk = kn.shape[2]
+    assert dn == 128 and qr.shape == (B, H, Tq, 64) and kn.shape == (B, H, Tk, 128)
+    assert kr.shape == (B, Tk, 64) and vv.shape == (B, H, Tk, 128)
+    kvl = None
+    if kv_len is not None:
+        kvl = np.ascontiguousarray(np.asarray(kv_len, dtype=np.int32).reshape(B))
+    if rows is None:
+        n = B * H * Tq
+        rows_arr = None
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1))
+        n = rows_arr.size
+    out = np.empty((n, 128), dtype=np.float64)
+    wsum = np.empty((n,), dtype=np.float64)
+    m = {"exact": 0, "eager": 1}[mode]
+    ptr = lambda a: None if a is None else a.ctypes.data  # noqa: E731
+    rc = lib.mla_oracle_rows(ptr(qn), ptr(qr), ptr(kn), ptr(kr), ptr(vv), ptr(kvl),
+                             B, H, Tq, Tk, int(past_len), float(softmax_scale), ptr(rows_arr), n,
+                             m, _threads(threads), ptr(out), ptr(wsum))
+    if rc != 0:
+        raise ValueError(f"oracle rejected its arguments (code {rc})")
+    return (out, wsum) if return_wsum else out
+
+
+def oracle_full(inp: dict, mode: str = "exact", threads: int | None = None) -> np.ndarray:
+    """All output rows for an input dict from the seeded generator, shaped [B,H,Tq,128]."""
+    B, H, Tq = inp["q_nope"].shape[:3]
+    o = oracle_rows(inp["q_nope"], inp["q_pe"], inp["k_nope"], inp["k_pe_shared"], inp["v"],
+                    inp["kv_len"], inp["past_len"], inp["softmax_scale"], mode=mode,
+                    threads=threads)
+    return o.reshape(B, H, Tq, 128)
+
+
+def round_bf16(x: float) -> float:
+    """The eager-emulation diagnostic's round-to-bf16 (exposed so a test can pin it)."""
+    return _load().mla_oracle_round_bf16(float(x))
