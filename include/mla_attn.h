@@ -1,0 +1,150 @@
+/*
+ * mla_attn.h -- C ABI of the GB300 (sm_103a) MLA causal-attention library.
+ *
+ * The operation is the causal-attention core of Kimi K2's Multi-head Latent Attention,
+ * as quoted on the page "Kimi K2 · Similarities" (section "Contextual evidence from
+ * Query-key similarity", the MLA forward of modeling_deepseek.py) and on the page
+ * "Weighted sum of values" (tensor card: weights [B,64,T,T] times values [B,64,T,128]
+ * give [B,64,T,128]).  Per sequence b, head h and query i:
+ *
+ *   Q   = [q_nope[b,h,i,0:128] | q_pe[b,h,i,0:64]]           (query concat)
+ *   K_j = [k_nope[b,h,j,0:128] | k_pe_shared[b,j,0:64]]      (key concat; one rotary
+ *                                                             key row shared by all heads)
+ *   s_j = softmax_scale * (Q . K_j)                          (scores, then scale)
+ *   key j is visible iff j <= i + past_len and j < kv_len[b] (4D causal mask offset by
+ *                                                             the cached length, plus
+ *                                                             right padding)
+ *   w   = softmax over visible j of s_j, in fp32             (hidden keys get weight 0)
+ *   out[b,h,i,:] = sum_j bf16(w_j) * v[b,h,j,:]              (weights cast to bf16, then
+ *                                                             the weighted sum of values)
+ *
+ * Dropout (attention_dropout = 0.0 in the config.json excerpt on "Kimi K2 · Logits") is
+ * the identity and is not applied.  The cache layout follows the cache update in the
+ * same excerpt: the Tk = past_len + Tq key/value rows hold the cached prefix first and
+ * the Tq new rows last, and query i sits at position past_len + i (positions are
+ * numbered from the cached length, page "Kimi K2 · Causal mask", section "Construct
+ * causal mask").
+ *
+ * Head widths are fixed by the config.json excerpt: qk_nope_head_dim 128,
+ * qk_rope_head_dim 64, v_head_dim 128.  The head count H is a runtime argument (64 in
+ * Kimi K2).
+ *
+ * Data types and layout.  bf16 tensors are passed as uint16_t bit patterns; every tensor
+ * is row-major and contiguous in the shape given, in DEVICE memory of the current CUDA
+ * device:
+ *   q_nope      [B, H, Tq, 128]      q_pe        [B, H, Tq, 64]
+ *   k_nope      [B, H, Tk, 128]      k_pe_shared [B, Tk, 64]
+ *   v           [B, H, Tk, 128]      out         [B, H, Tq, 128]
+ *   kv_len      [B] int32, or NULL meaning kv_len[b] = Tk for every b
+ * Every pointer must be 16-byte aligned (bulk/tensor copies move 16-byte units).
+ *
+ * Ownership.  The caller owns every buffer: inputs, out, kv_len and the workspace.  The
+ * library never allocates or frees device memory on the call path.  Inputs are only
+ * read; out is fully overwritten.  Work is enqueued asynchronously on cuda_stream (a
+ * cudaStream_t, NULL for the legacy default stream); the call returns before it runs.
+ *
+ * Errors.  Host-side checks run before anything is enqueued and are returned directly
+ * (nothing is launched when a check fails).  Problems only the device can see
+ * (kv_len[b] outside [1, Tk]; a bounded wait that gave up) are recorded in a status word
+ * inside the workspace; mla_attn_get_status reads it.  Such a call still completes: an
+ * out-of-range kv_len is clamped to [1, Tk] for memory safety and the output for that
+ * sequence is not meaningful.
+ */
+#ifndef MLA_ATTN_H_
+#define MLA_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MLA_API __attribute__((visibility("default")))
+#else
+#define MLA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_NULL = 1,      /* a required pointer is NULL */
+  MLA_ERR_SHAPE = 2,     /* B, H, Tq < 1, past_len < 0, Tk != past_len + Tq, or too large:
+                            the score-shape check of the attention excerpt (scores must be
+                            [B, H, Tq, Tk]) */
+  MLA_ERR_ALIGN = 3,     /* a pointer is not 16-byte aligned */
+  MLA_ERR_WORKSPACE = 4, /* workspace NULL or smaller than mla_attn_workspace_bytes() */
+  MLA_ERR_DEVICE = 5,    /* the current device is not an sm_103 (GB300-class) GPU */
+  MLA_ERR_CUDA = 6,      /* a CUDA runtime call or kernel launch failed */
+  MLA_ERR_KVLEN = 7,     /* (device) some kv_len[b] outside [1, Tk] */
+  MLA_ERR_TIMEOUT = 8,   /* (device) a bounded wait inside a kernel gave up */
+  MLA_ERR_ARG = 9        /* an option value is out of range */
+} mla_status;
+
+/*
+ * Bytes of device workspace mla_attn_fwd needs for these sizes (a status word plus the
+ * split-KV partial results of the decode path).  The workspace must be zero-filled once
+ * before its first use (cudaMemset); afterwards the library keeps the status word
+ * consistent itself.  Returns 0 for invalid sizes.
+ */
+MLA_API size_t mla_attn_workspace_bytes(int B, int H, int Tq, int Tk);
+
+/*
+ * The attention core described at the top of this file.  past_len is the cached length
+ * (Tk must equal past_len + Tq); softmax_scale (finite, > 0, else MLA_ERR_ARG) multiplies
+ * the raw scores (192^-0.5 for Kimi K2 before any YaRN adjustment, which the caller folds
+ * in).  Tq == 1 takes the
+ * split-KV decode path; Tq > 1 the tensor-core prefill path.  Returns MLA_OK once the
+ * work is enqueued, or a host-side error code.
+ */
+MLA_API mla_status mla_attn_fwd(const uint16_t* q_nope, const uint16_t* q_pe, const uint16_t* k_nope,
+                        const uint16_t* k_pe_shared, const uint16_t* v, const int32_t* kv_len,
+                        int B, int H, int Tq, int Tk, int past_len, float softmax_scale,
+                        uint16_t* out, void* workspace, size_t workspace_bytes,
+                        void* cuda_stream);
+
+/* Path selection for mla_attn_fwd_ex. */
+typedef enum { MLA_PATH_AUTO = 0, MLA_PATH_PREFILL = 1, MLA_PATH_DECODE = 2 } mla_path;
+
+/*
+ * Options for mla_attn_fwd_ex.  Zero-initialised options mean "choose automatically",
+ * which is what mla_attn_fwd does.
+ *   path:         force the prefill (any Tq >= 1) or decode (Tq == 1 only) path.
+ *   decode_chunk: keys per split of the decode path (a multiple of 64, at most 65536);
+ *                 0 lets the scheduler pick it from B, H and Tk.
+ */
+typedef struct {
+  int path;
+  int decode_chunk;
+  int reserved[6];
+} mla_attn_options;
+
+/* mla_attn_fwd with explicit options (same arguments and semantics otherwise). */
+MLA_API mla_status mla_attn_fwd_ex(const uint16_t* q_nope, const uint16_t* q_pe,
+                           const uint16_t* k_nope, const uint16_t* k_pe_shared,
+                           const uint16_t* v, const int32_t* kv_len, int B, int H, int Tq,
+                           int Tk, int past_len, float softmax_scale, uint16_t* out,
+                           void* workspace, size_t workspace_bytes, void* cuda_stream,
+                           const mla_attn_options* options);
+
+/*
+ * Synchronises cuda_stream, reads the device status word in the workspace, clears it,
+ * and returns it (MLA_OK if no kernel recorded a problem since the last read).
+ */
+MLA_API mla_status mla_attn_get_status(void* workspace, void* cuda_stream);
+
+/* Static, human-readable name of a status code. */
+MLA_API const char* mla_status_string(mla_status status);
+
+/*
+ * The decode scheduler's choice for these sizes: keys per split and number of splits
+ * (written through the non-NULL pointers).  Pure host arithmetic; returns MLA_ERR_SHAPE
+ * for invalid sizes.
+ */
+MLA_API mla_status mla_attn_decode_plan(int B, int H, int Tk, int* chunk, int* splits);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_ATTN_H_ */

@@ -1,0 +1,191 @@
+"""ctypes binding of libmla_attn.so (argument marshalling only).
+
+Every step of the attention core runs in the library's CUDA kernels; this module only
+checks tensor dtypes/devices, passes raw device pointers, sizes and the current CUDA
+stream, and turns status codes into exceptions.  There is no fallback: if the library is
+missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import enum
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libmla_attn.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class MlaStatus(enum.IntEnum):
+    OK = 0
+    ERR_NULL = 1
+    ERR_SHAPE = 2
+    ERR_ALIGN = 3
+    ERR_WORKSPACE = 4
+    ERR_DEVICE = 5
+    ERR_CUDA = 6
+    ERR_KVLEN = 7
+    ERR_TIMEOUT = 8
+    ERR_ARG = 9
+
+
+PATH_AUTO, PATH_PREFILL, PATH_DECODE = 0, 1, 2
+
+
+class MlaAttnError(RuntimeError):
+    def __init__(self, status: int, msg: str = ""):
+        self.status = MlaStatus(status) if status in MlaStatus._value2member_map_ else status
+        super().__init__(f"{msg}{self.status!r}: {_status_string(status)}")
+
+
+class _Options(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int), ("decode_chunk", ctypes.c_int),
+                ("reserved", ctypes.c_int * 6)]
+
+
+EXPORTED = ("mla_attn_workspace_bytes", "mla_attn_fwd", "mla_attn_fwd_ex",
+            "mla_attn_get_status", "mla_status_string", "mla_attn_decode_plan")
+
+
+def library():
+    """Load libmla_attn.so (built in-tree by build.py); raise if it is not there."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise MlaAttnError(MlaStatus.ERR_CUDA,
+                               f"{LIB_PATH} is not built (run python -m "
+                               "mla_causal_attention_gb300.build); ")
+        lib = ctypes.CDLL(LIB_PATH)
+        p, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        fwd_args = [p, p, p, p, p, p, i, i, i, i, i, f, p, p, sz, p]
+        lib.mla_attn_workspace_bytes.restype = sz
+        lib.mla_attn_workspace_bytes.argtypes = [i, i, i, i]
+        lib.mla_attn_fwd.restype = i
+        lib.mla_attn_fwd.argtypes = fwd_args
+        lib.mla_attn_fwd_ex.restype = i
+        lib.mla_attn_fwd_ex.argtypes = fwd_args + [ctypes.POINTER(_Options)]
+        lib.mla_attn_get_status.restype = i
+        lib.mla_attn_get_status.argtypes = [p, p]
+        lib.mla_status_string.restype = ctypes.c_char_p
+        lib.mla_status_string.argtypes = [i]
+        lib.mla_attn_decode_plan.restype = i
+        lib.mla_attn_decode_plan.argtypes = [i, i, i, ctypes.POINTER(i), ctypes.POINTER(i)]
+        _lib = lib
+        return lib
+
+
+def _status_string(s: int) -> str:
+    try:
+        return library().mla_status_string(int(s)).decode()
+    except Exception:  # pragma: no cover - library missing
+        return "libmla_attn.so unavailable"
+
+
+def mla_attn_workspace_bytes(B: int, H: int, Tq: int, Tk: int) -> int:
+    return int(library().mla_attn_workspace_bytes(B, H, Tq, Tk))
+
+
+def decode_plan(B: int, H: int, Tk: int):
+    c, s = ctypes.c_int(), ctypes.c_int()
+    rc = library().mla_attn_decode_plan(B, H, Tk, ctypes.byref(c), ctypes.byref(s))
+    if rc != 0:
+        raise MlaAttnError(rc)
+    return c.value, s.value
+
+
+class Workspace:
+    """A zero-initialised device workspace sized for given shapes (grows on demand)."""
+
+    def __init__(self, device=None):
+        self.device = torch.device(device or "cuda")
+        self.buf = None
+
+    def get(self, nbytes: int) -> torch.Tensor:
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+        return self.buf
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(t, name, dtype, shape, device):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def mla_attn_fwd(q_nope, q_pe, k_nope, k_pe_shared, v, kv_len, past_len: int,
+                 softmax_scale: float, out=None, workspace: Workspace | None = None,
+                 stream=None, path: int = PATH_AUTO, decode_chunk: int = 0):
+    """out[B,H,Tq,128] (bf16) of the MLA causal-attention core on the current device.
+
+    q_nope [B,H,Tq,128], q_pe [B,H,Tq,64], k_nope [B,H,Tk,128], k_pe_shared [B,Tk,64],
+    v [B,H,Tk,128] (bf16, contiguous, CUDA); kv_len [B] int32 on the same device or None.
+    Enqueued on ``stream`` (default: torch's current stream); returns ``out``.
+    """
+    lib = library()
+    dev = q_nope.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    B, H, Tq = q_nope.shape[:3]
+    Tk = k_nope.shape[2]
+    bf = torch.bfloat16
+    _check(q_nope, "q_nope", bf, (B, H, Tq, 128), dev)
+    _check(q_pe, "q_pe", bf, (B, H, Tq, 64), dev)
+    _check(k_nope, "k_nope", bf, (B, H, Tk, 128), dev)
+    _check(k_pe_shared, "k_pe_shared", bf, (B, Tk, 64), dev)
+    _check(v, "v", bf, (B, H, Tk, 128), dev)
+    if kv_len is not None:
+        _check(kv_len, "kv_len", torch.int32, (B,), dev)
+    if out is None:
+        out = torch.empty((B, H, Tq, 128), dtype=bf, device=dev)
+    _check(out, "out", bf, (B, H, Tq, 128), dev)
+    ws_bytes = lib.mla_attn_workspace_bytes(B, H, Tq, Tk)
+    if decode_chunk:
+        ws_bytes = max(ws_bytes, 256 + B * H * (-(-Tk // decode_chunk)) * 130 * 4)
+    ws = (workspace or _default_workspace(dev)).get(ws_bytes)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    handle = ctypes.c_void_p(s.cuda_stream)
+    opts = _Options(int(path), int(decode_chunk))
+    with torch.cuda.device(dev):
+        rc = lib.mla_attn_fwd_ex(_ptr(q_nope), _ptr(q_pe), _ptr(k_nope), _ptr(k_pe_shared),
+                                 _ptr(v), _ptr(kv_len), B, H, Tq, Tk, int(past_len),
+                                 float(softmax_scale), _ptr(out), _ptr(ws), ws.numel(),
+                                 handle, ctypes.byref(opts))
+    if rc != 0:
+        raise MlaAttnError(rc, "mla_attn_fwd: ")
+    return out
+
+
+def mla_attn_get_status(workspace: Workspace | None = None, device=None, stream=None) -> int:
+    """Synchronise and read/clear the device status word (0 = no device-side error)."""
+    dev = torch.device(device or "cuda")
+    ws = (workspace or _default_workspace(dev)).get(256)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        return int(library().mla_attn_get_status(_ptr(ws), ctypes.c_void_p(s.cuda_stream)))
+
+
+_default_ws: dict = {}
+
+
+def _default_workspace(dev) -> Workspace:
+    key = str(dev)
+    if key not in _default_ws:
+        _default_ws[key] = Workspace(dev)
+    return _default_ws[key]

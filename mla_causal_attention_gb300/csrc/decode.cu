@@ -1,0 +1,339 @@
+// decode.cu -- split-KV decode kernel (Tq == 1) and its combine pass, sm_103a.
+//
+// Per sequence b and head h the single query attends to keys j < kv_len[b]:
+//   s_j = softmax_scale * ([q_nope | q_pe] . [k_nope[b,h,j] | k_pe_shared[b,j]])
+//   out = sum_j softmax(s)_j v[b,h,j]
+// (the attention excerpt on "Kimi K2 · Similarities"; with Tq = 1 and Tk = past_len + 1
+// the causal limit admits every cached key, so only kv_len hides keys).
+//
+// Work split: one CTA per (group of 4 heads, key chunk, sequence).  One producer thread
+// streams each 32-key stage with 1-D bulk copies into a 3-deep shared-memory ring: the
+// shared rotary-key rows once per stage, then the no-rope key and value rows of the four
+// heads.  Two consumer warps per head split the stage's keys: 8 lanes per key form the
+// 192-wide dot product (128-bit shared loads, 3 shuffles), the warp keeps a running
+// (max, sum) in the log2 domain, and every lane accumulates 4 output columns.  The CTA
+// writes either the final bf16 row (single split) or a (max, sum, acc[128]) partial that
+// the combine kernel merges:  m = max m_s,  l = sum 2^(m_s - m) l_s,
+// out = sum 2^(m_s - m) acc_s / l.
+#include <cmath>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace mla {
+namespace {
+
+template <int G, int T, int NST, int WPH>
+struct DecCfg {
+  static constexpr int kConsumerWarps = G * WPH;
+  static constexpr int kThreads = (kConsumerWarps + 1) * 32;
+  static constexpr int kTokPerWarp = T / WPH;
+  static constexpr int kPasses = kTokPerWarp / 4;
+  static constexpr uint32_t kKpeBytes = T * 128;
+  static constexpr uint32_t kKnBytes = T * 256;
+  static constexpr uint32_t kVBytes = T * 256;
+  static constexpr uint32_t kStageBytes = kKpeBytes + G * (kKnBytes + kVBytes);
+  static constexpr uint32_t kMergeBytes = kConsumerWarps * 132 * 4;
+  static constexpr uint32_t kBarBytes = 128;
+  static constexpr uint32_t kSmemBytes = NST * kStageBytes + kMergeBytes + kBarBytes;
+  static_assert(T % (4 * WPH) == 0, "stage keys must split into 4-key passes per warp");
+  static_assert(kStageBytes % 128 == 0, "stage alignment");
+};
+
+__device__ __forceinline__ float dot8(const uint4 k, const float* q) {
+  float s = 0.f;
+  s = fmaf(q[0], bf16lo_to_f32(k.x), s);
+  s = fmaf(q[1], bf16hi_to_f32(k.x), s);
+  s = fmaf(q[2], bf16lo_to_f32(k.y), s);
+  s = fmaf(q[3], bf16hi_to_f32(k.y), s);
+  s = fmaf(q[4], bf16lo_to_f32(k.z), s);
+  s = fmaf(q[5], bf16hi_to_f32(k.z), s);
+  s = fmaf(q[6], bf16lo_to_f32(k.w), s);
+  s = fmaf(q[7], bf16hi_to_f32(k.w), s);
+  return s;
+}
+
+__device__ __forceinline__ void load8(const uint16_t* src, float scale, float* dst) {
+  const uint4 w = *reinterpret_cast<const uint4*>(src);
+  dst[0] = bf16lo_to_f32(w.x) * scale;
+  dst[1] = bf16hi_to_f32(w.x) * scale;
+  dst[2] = bf16lo_to_f32(w.y) * scale;
+  dst[3] = bf16hi_to_f32(w.y) * scale;
+  dst[4] = bf16lo_to_f32(w.z) * scale;
+  dst[5] = bf16hi_to_f32(w.z) * scale;
+  dst[6] = bf16lo_to_f32(w.w) * scale;
+  dst[7] = bf16hi_to_f32(w.w) * scale;
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Bounded wait used only to drain the producer's own copies before exit; ignores the
+// abort flag (copies in flight must land before the CTA's shared memory goes away).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(a, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+template <int G, int T, int NST, int WPH>
+__global__ void __launch_bounds__(DecCfg<G, T, NST, WPH>::kThreads, 1)
+    decode_splitkv_kernel(const DecodeArgs p) {
+  using C = DecCfg<G, T, NST, WPH>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* stages = smem;
+  float* merge = reinterpret_cast<float*>(smem + NST * C::kStageBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NST * C::kStageBytes + C::kMergeBytes);
+  uint64_t* empty = full + NST;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + NST);
+
+  const int hg = blockIdx.x;
+  const int split = blockIdx.y;
+  const int b = blockIdx.z;
+  const int h0 = hg * G;
+  const int ng = min(G, p.H - h0);
+
+  int kvl = p.kv_len ? p.kv_len[b] : p.Tk;
+  if (kvl < 1 || kvl > p.Tk) {
+    if (threadIdx.x == 0 && hg == 0 && split == 0) set_status(p.status, MLA_ERR_KVLEN);
+    kvl = min(max(kvl, 1), p.Tk);
+  }
+  const int j0 = split * p.chunk;
+  if (j0 >= kvl) return;  // uniform across the CTA: this split holds no visible key
+  const int j1 = min(j0 + p.chunk, kvl);
+  const int n_tiles = (j1 - j0 + T - 1) / T;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], C::kConsumerWarps);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == C::kConsumerWarps) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_first();
+      const uint64_t pol_kpe = l2_policy_evict_last();  // re-read by the other head groups
+      int issued = 0;
+      for (int it = 0; it < n_tiles; ++it) {
+        const int slot = it % NST;
+        if (it >= NST) {
+          if (!mbar_wait(&empty[slot], ((it / NST) - 1) & 1, p.status, abort_flag)) break;
+        }
+        const int jt = j0 + it * T;
+        const int nt = min(T, j1 - jt);
+        uint8_t* st = stages + slot * C::kStageBytes;
+        mbar_arrive_expect_tx(&full[slot], (uint32_t)nt * (128u + (uint32_t)ng * 512u));
+        bulk_g2s(st, p.k_pe + ((size_t)b * p.Tk + jt) * 64, nt * 128, &full[slot], pol_kpe);
+        for (int g = 0; g < ng; ++g) {
+          const size_t bh = (size_t)b * p.H + h0 + g;
+          bulk_g2s(st + C::kKpeBytes + g * C::kKnBytes, p.k_nope + (bh * p.Tk + jt) * 128,
+                   nt * 256, &full[slot], pol);
+          bulk_g2s(st + C::kKpeBytes + G * C::kKnBytes + g * C::kVBytes,
+                   p.v + (bh * p.Tk + jt) * 128, nt * 256, &full[slot], pol);
+        }
+        ++issued;
+      }
+      // Let every copy this thread issued land before the CTA can exit.
+      for (int it = max(0, issued - NST); it < issued; ++it)
+        drain_wait(&full[it % NST], (it / NST) & 1);
+    }
+    return;
+  }
+
+  // ---------------- consumers ----------------
+  const int g = warp / WPH;
+  const int wh = warp % WPH;
+  const bool head_ok = g < ng;
+  const int l8 = lane & 7;
+  const int tk = lane >> 3;
+  const size_t bh = (size_t)b * p.H + h0 + (head_ok ? g : 0);
+
+  // This lane's slice of the query, pre-multiplied by softmax_scale * log2(e): 16 of the
+  // 128 no-rope columns and 8 of the 64 rotary columns.
+  float qn[16], qr[8];
+  {
+    const uint16_t* qsrc = p.q_nope + bh * 128 + l8 * 16;
+    load8(qsrc, p.scale_log2, qn);
+    load8(qsrc + 8, p.scale_log2, qn + 8);
+    load8(p.q_pe + bh * 64 + l8 * 8, p.scale_log2, qr);
+  }
+
+  float m_run = -1e30f;  // finite sentinel: 2^(m_run - m_new) stays defined
+  float l_run = 0.f;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+
+  for (int it = 0; it < n_tiles; ++it) {
+    const int slot = it % NST;
+    if (!mbar_wait(&full[slot], (it / NST) & 1, p.status, abort_flag)) break;
+    const int jt = j0 + it * T;
+    const int nt = min(T, j1 - jt);
+    if (head_ok) {
+      const uint8_t* st = stages + slot * C::kStageBytes;
+      const uint8_t* kpe_s = st;
+      const uint8_t* kn_s = st + C::kKpeBytes + g * C::kKnBytes;
+      const uint8_t* v_s = st + C::kKpeBytes + G * C::kKnBytes + g * C::kVBytes;
+
+      float sc[C::kPasses];
+#pragma unroll
+      for (int ps = 0; ps < C::kPasses; ++ps) {
+        const int t = wh * C::kTokPerWarp + ps * 4 + tk;
+        const uint8_t* krow = kn_s + t * 256 + l8 * 32;
+        const uint4 a0 = *reinterpret_cast<const uint4*>(krow);
+        const uint4 a1 = *reinterpret_cast<const uint4*>(krow + 16);
+        const uint4 c0 = *reinterpret_cast<const uint4*>(kpe_s + t * 128 + l8 * 16);
+        float d = dot8(a0, qn) + dot8(a1, qn + 8) + dot8(c0, qr);
+        d += __shfl_xor_sync(0xffffffffu, d, 1);
+        d += __shfl_xor_sync(0xffffffffu, d, 2);
+        d += __shfl_xor_sync(0xffffffffu, d, 4);
+        sc[ps] = (t < nt) ? d : -INFINITY;
+      }
+      float mx = sc[0];
+#pragma unroll
+      for (int ps = 1; ps < C::kPasses; ++ps) mx = fmaxf(mx, sc[ps]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float m_new = fmaxf(m_run, mx);
+      const float alpha = ex2_approx(m_run - m_new);
+      float pr[C::kPasses];
+      float ps_sum = 0.f;
+#pragma unroll
+      for (int ps = 0; ps < C::kPasses; ++ps) {
+        pr[ps] = ex2_approx(sc[ps] - m_new);
+        ps_sum += pr[ps];
+      }
+      ps_sum += __shfl_xor_sync(0xffffffffu, ps_sum, 8);
+      ps_sum += __shfl_xor_sync(0xffffffffu, ps_sum, 16);
+      l_run = l_run * alpha + ps_sum;
+      m_run = m_new;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[c] *= alpha;
+      // Value mix: lane owns columns [4*lane, 4*lane + 4).
+#pragma unroll
+      for (int tt = 0; tt < C::kTokPerWarp; ++tt) {
+        const int t = wh * C::kTokPerWarp + tt;
+        const float pt = __shfl_sync(0xffffffffu, pr[tt / 4], (tt % 4) * 8);
+        if (t < nt) {
+          const uint2 vv = *reinterpret_cast<const uint2*>(v_s + t * 256 + lane * 8);
+          acc[0] = fmaf(pt, bf16lo_to_f32(vv.x), acc[0]);
+          acc[1] = fmaf(pt, bf16hi_to_f32(vv.x), acc[1]);
+          acc[2] = fmaf(pt, bf16lo_to_f32(vv.y), acc[2]);
+          acc[3] = fmaf(pt, bf16hi_to_f32(vv.y), acc[3]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+  }
+
+  // Merge the WPH warps of each head through shared memory.
+  float* mw = merge + warp * 132;
+  if (lane == 0) {
+    mw[0] = m_run;
+    mw[1] = l_run;
+  }
+  *reinterpret_cast<float4*>(mw + 4 + lane * 4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  named_bar_sync(1, C::kConsumerWarps * 32);
+  if (wh != 0 || !head_ok || *abort_flag) return;
+
+  float m = -1e30f;
+#pragma unroll
+  for (int w = 0; w < WPH; ++w) m = fmaxf(m, merge[(warp + w) * 132]);
+  float l = 0.f;
+  float o[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int w = 0; w < WPH; ++w) {
+    const float* src = merge + (warp + w) * 132;
+    const float f = ex2_approx(src[0] - m);
+    l += f * src[1];
+    const float4 a = *reinterpret_cast<const float4*>(src + 4 + lane * 4);
+    o[0] += f * a.x;
+    o[1] += f * a.y;
+    o[2] += f * a.z;
+    o[3] += f * a.w;
+  }
+  if (p.splits == 1) {
+    const float inv = 1.f / l;
+    uint2 w;
+    w.x = pack_bf16x2(o[0] * inv, o[1] * inv);
+    w.y = pack_bf16x2(o[2] * inv, o[3] * inv);
+    *reinterpret_cast<uint2*>(p.out + bh * 128 + lane * 4) = w;
+  } else {
+    const size_t pi = bh * p.splits + split;
+    if (lane == 0) *reinterpret_cast<float2*>(p.part_ml + pi * 2) = make_float2(m, l);
+    *reinterpret_cast<float4*>(p.part_acc + pi * 128 + lane * 4) =
+        make_float4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// One warp per (b, h): merge the partials of the splits that hold visible keys.
+__global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeArgs p) {
+  const int w = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (w >= p.B * p.H) return;
+  const int b = w / p.H;
+  int kvl = p.kv_len ? p.kv_len[b] : p.Tk;
+  kvl = min(max(kvl, 1), p.Tk);
+  const int n = (kvl + p.chunk - 1) / p.chunk;
+  const size_t base = (size_t)w * p.splits;
+  float m = -1e30f;
+  for (int s = lane; s < n; s += 32) m = fmaxf(m, p.part_ml[(base + s) * 2]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float l = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < n; ++s) {
+    const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + (base + s) * 2);
+    const float f = ex2_approx(ml.x - m);
+    l += f * ml.y;
+    const float4 a = *reinterpret_cast<const float4*>(p.part_acc + (base + s) * 128 + lane * 4);
+    acc.x += f * a.x;
+    acc.y += f * a.y;
+    acc.z += f * a.z;
+    acc.w += f * a.w;
+  }
+  const float inv = 1.f / l;
+  uint2 o;
+  o.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+  o.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+  *reinterpret_cast<uint2*>(p.out + (size_t)w * 128 + lane * 4) = o;
+}
+
+using DecKernelCfg = DecCfg<kDecHeadsPerCta, kDecTokensPerStage, 3, 2>;
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
+  constexpr int G = kDecHeadsPerCta, T = kDecTokensPerStage, NST = 3, WPH = 2;
+  using C = DecCfg<G, T, NST, WPH>;
+  auto kern = decode_splitkv_kernel<G, T, NST, WPH>;
+  static int attr_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (attr_device != dev) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_device = dev;
+  }
+  dim3 grid((a.H + G - 1) / G, a.splits, a.B);
+  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || a.splits == 1) return e;
+  const int warps = a.B * a.H;
+  decode_combine_kernel<<<(warps + 7) / 8, 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -1,0 +1,205 @@
+// host.cu -- the C ABI of libmla_attn.so: argument checks, workspace layout, the decode
+// split scheduler, kernel launches and the device status word.
+//
+// The checks mirror the guards of the attention excerpt on "Kimi K2 · Similarities":
+// the scores must have shape [B, H, Tq, Tk] with Tk the cached length plus the new
+// rows, and a mask must be present (here it is implied by past_len and kv_len, so it is
+// always present).  Failing checks return an error code; nothing is launched.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "kernels.h"
+#include "mla_attn.h"
+
+namespace mla {
+namespace {
+
+constexpr size_t kStatusBytes = 256;  // status word + padding at the start of the workspace
+constexpr int kMaxDevices = 64;
+constexpr int64_t kMaxElems = int64_t(1) << 40;
+
+// 0 = unknown, 1 = sm_103, 2 = other.  Per device, filled on first use.
+std::atomic<int> g_dev_kind[kMaxDevices];
+std::atomic<int> g_dev_sms[kMaxDevices];
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+mla_status check_device(int* sms_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MLA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return MLA_ERR_DEVICE;
+  int kind = g_dev_kind[dev].load(std::memory_order_acquire);
+  if (kind == 0) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MLA_ERR_CUDA;
+    kind = (major == 10 && minor == 3) ? 1 : 2;
+    g_dev_sms[dev].store(sms, std::memory_order_relaxed);
+    g_dev_kind[dev].store(kind, std::memory_order_release);
+  }
+  if (kind != 1) return MLA_ERR_DEVICE;
+  if (sms_out) *sms_out = g_dev_sms[dev].load(std::memory_order_relaxed);
+  return MLA_OK;
+}
+
+mla_status check_shape(int B, int H, int Tq, int Tk, int past_len) {
+  if (B < 1 || H < 1 || Tq < 1 || past_len < 0) return MLA_ERR_SHAPE;
+  if ((int64_t)past_len + Tq != (int64_t)Tk) return MLA_ERR_SHAPE;
+  if ((int64_t)B * H * Tk * 128 > kMaxElems) return MLA_ERR_SHAPE;
+  if (B > 65535) return MLA_ERR_SHAPE;  // grid z of the decode launch
+  return MLA_OK;
+}
+
+// Keys per split for the decode path: the largest power-of-two multiple of 64 (at most
+// 1024) that still leaves two full waves of CTAs on the GPU at one CTA per SM.
+void plan_decode(int B, int H, int Tk, int sms, int* chunk, int* splits) {
+  const int64_t groups = (int64_t)B * ((H + kDecHeadsPerCta - 1) / kDecHeadsPerCta);
+  int c = kDecMinChunk;
+  while (c < 1024) {
+    const int64_t next = groups * ((Tk + 2 * c - 1) / (2 * c));
+    if (next < 2 * (int64_t)sms) break;
+    c *= 2;
+  }
+  *chunk = c;
+  *splits = (Tk + c - 1) / c;
+}
+
+size_t decode_workspace(int B, int H, int splits) {
+  if (splits <= 1) return kStatusBytes;
+  return kStatusBytes + (size_t)B * H * splits * (2 + 128) * sizeof(float);
+}
+
+}  // namespace
+
+int device_sm_count() {
+  int sms = 0;
+  return check_device(&sms) == MLA_OK ? sms : 0;
+}
+
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" {
+
+const char* mla_status_string(mla_status s) {
+  switch (s) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_NULL: return "MLA_ERR_NULL: a required pointer is NULL";
+    case MLA_ERR_SHAPE: return "MLA_ERR_SHAPE: invalid sizes (need B,H,Tq>=1, past_len>=0, Tk==past_len+Tq)";
+    case MLA_ERR_ALIGN: return "MLA_ERR_ALIGN: a pointer is not 16-byte aligned";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE: workspace missing or too small";
+    case MLA_ERR_DEVICE: return "MLA_ERR_DEVICE: current device is not sm_103";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA: CUDA runtime or launch failure";
+    case MLA_ERR_KVLEN: return "MLA_ERR_KVLEN: kv_len[b] outside [1, Tk]";
+    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT: a bounded wait in a kernel gave up";
+    case MLA_ERR_ARG: return "MLA_ERR_ARG: option out of range";
+  }
+  return "unknown mla_status";
+}
+
+mla_status mla_attn_decode_plan(int B, int H, int Tk, int* chunk, int* splits) {
+  if (B < 1 || H < 1 || Tk < 1) return MLA_ERR_SHAPE;
+  int sms = 0;
+  if (check_device(&sms) != MLA_OK || sms <= 0) sms = 152;  // GB300 SM count when no device
+  int c = 0, s = 0;
+  plan_decode(B, H, Tk, sms, &c, &s);
+  if (chunk) *chunk = c;
+  if (splits) *splits = s;
+  return MLA_OK;
+}
+
+size_t mla_attn_workspace_bytes(int B, int H, int Tq, int Tk) {
+  if (B < 1 || H < 1 || Tq < 1 || Tk < Tq) return 0;
+  if (Tq != 1) return kStatusBytes;
+  int c = 0, s = 0;
+  mla_attn_decode_plan(B, H, Tk, &c, &s);
+  return decode_workspace(B, H, s);
+}
+
+mla_status mla_attn_fwd_ex(const uint16_t* q_nope, const uint16_t* q_pe,
+                           const uint16_t* k_nope, const uint16_t* k_pe_shared,
+                           const uint16_t* v, const int32_t* kv_len, int B, int H, int Tq,
+                           int Tk, int past_len, float softmax_scale, uint16_t* out,
+                           void* workspace, size_t workspace_bytes, void* cuda_stream,
+                           const mla_attn_options* options) {
+  if (!q_nope || !q_pe || !k_nope || !k_pe_shared || !v || !out) return MLA_ERR_NULL;
+  if (!workspace) return MLA_ERR_WORKSPACE;
+  mla_status st = check_shape(B, H, Tq, Tk, past_len);
+  if (st != MLA_OK) return st;
+  if (!aligned16(q_nope) || !aligned16(q_pe) || !aligned16(k_nope) || !aligned16(k_pe_shared) ||
+      !aligned16(v) || !aligned16(out) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(kv_len) & 3u) != 0)
+    return MLA_ERR_ALIGN;
+  if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.0f)) return MLA_ERR_ARG;
+  int path = options ? options->path : MLA_PATH_AUTO;
+  if (path < MLA_PATH_AUTO || path > MLA_PATH_DECODE) return MLA_ERR_ARG;
+  if (path == MLA_PATH_AUTO) path = (Tq == 1) ? MLA_PATH_DECODE : MLA_PATH_PREFILL;
+  if (path == MLA_PATH_DECODE && Tq != 1) return MLA_ERR_ARG;
+  int sms = 0;
+  st = check_device(&sms);
+  if (st != MLA_OK) return st;
+
+  cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+  int* status = static_cast<int*>(workspace);
+  const float scale_log2 = softmax_scale * 1.4426950408889634f;
+
+  if (path == MLA_PATH_DECODE) {
+    int chunk = 0, splits = 0;
+    plan_decode(B, H, Tk, sms, &chunk, &splits);
+    const int forced = options ? options->decode_chunk : 0;
+    if (forced != 0) {
+      if (forced < kDecMinChunk || forced > kDecMaxChunk || forced % kDecMinChunk != 0)
+        return MLA_ERR_ARG;
+      chunk = forced;
+      splits = (Tk + chunk - 1) / chunk;
+    }
+    if (splits > 65535) return MLA_ERR_ARG;
+    if (workspace_bytes < decode_workspace(B, H, splits)) return MLA_ERR_WORKSPACE;
+    DecodeArgs a;
+    a.q_nope = q_nope; a.q_pe = q_pe; a.k_nope = k_nope; a.k_pe = k_pe_shared; a.v = v;
+    a.kv_len = kv_len; a.out = out; a.status = status;
+    float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kStatusBytes);
+    a.part_ml = part;
+    a.part_acc = part + (size_t)B * H * splits * 2;
+    a.B = B; a.H = H; a.Tk = Tk; a.chunk = chunk; a.splits = splits;
+    a.scale_log2 = scale_log2;
+    return launch_decode(a, stream) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+  }
+
+  if (workspace_bytes < kStatusBytes) return MLA_ERR_WORKSPACE;
+  PrefillArgs a;
+  a.q_nope = q_nope; a.q_pe = q_pe; a.k_nope = k_nope; a.k_pe = k_pe_shared; a.v = v;
+  a.kv_len = kv_len; a.out = out; a.status = status;
+  a.B = B; a.H = H; a.Tq = Tq; a.Tk = Tk; a.past_len = past_len;
+  a.scale_log2 = scale_log2;
+  return launch_prefill(a, stream) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+mla_status mla_attn_fwd(const uint16_t* q_nope, const uint16_t* q_pe, const uint16_t* k_nope,
+                        const uint16_t* k_pe_shared, const uint16_t* v, const int32_t* kv_len,
+                        int B, int H, int Tq, int Tk, int past_len, float softmax_scale,
+                        uint16_t* out, void* workspace, size_t workspace_bytes,
+                        void* cuda_stream) {
+  return mla_attn_fwd_ex(q_nope, q_pe, k_nope, k_pe_shared, v, kv_len, B, H, Tq, Tk, past_len,
+                         softmax_scale, out, workspace, workspace_bytes, cuda_stream, nullptr);
+}
+
+mla_status mla_attn_get_status(void* workspace, void* cuda_stream) {
+  if (!workspace) return MLA_ERR_WORKSPACE;
+  cudaStream_t stream = static_cast<cudaStream_t>(cuda_stream);
+  int host = 0;
+  if (cudaMemcpyAsync(&host, workspace, sizeof(int), cudaMemcpyDeviceToHost, stream) !=
+      cudaSuccess)
+    return MLA_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, sizeof(int), stream) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MLA_ERR_CUDA;
+  if (host < 0 || host > MLA_ERR_ARG) return MLA_ERR_CUDA;
+  return static_cast<mla_status>(host);
+}
+
+}  // extern "C"

@@ -1,0 +1,56 @@
+// kernels.h -- internal launch interface between the C-ABI host code and the kernels.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mla {
+
+// Decode (Tq == 1): split-KV partial pass, then a combine pass when there are several
+// splits.  Partials live in the caller's workspace: part_ml [B*H*splits][2] = (max, sum)
+// in the log2 domain, part_acc [B*H*splits][128] = unnormalised weighted value sums.
+struct DecodeArgs {
+  const uint16_t* q_nope;
+  const uint16_t* q_pe;
+  const uint16_t* k_nope;
+  const uint16_t* k_pe;
+  const uint16_t* v;
+  const int32_t* kv_len;  // may be null
+  uint16_t* out;
+  float* part_ml;
+  float* part_acc;
+  int* status;
+  int B, H, Tk;
+  int chunk;   // keys per split (multiple of the stage size)
+  int splits;  // ceil(Tk / chunk)
+  float scale_log2;  // softmax_scale * log2(e)
+};
+
+// Decode kernel configuration (shared with the scheduler).
+constexpr int kDecHeadsPerCta = 4;   // heads sharing one rotary-key tile
+constexpr int kDecTokensPerStage = 32;
+constexpr int kDecMinChunk = 64;
+constexpr int kDecMaxChunk = 65536;
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+// Prefill (Tq >= 1): fused tensor-core kernel.
+struct PrefillArgs {
+  const uint16_t* q_nope;
+  const uint16_t* q_pe;
+  const uint16_t* k_nope;
+  const uint16_t* k_pe;
+  const uint16_t* v;
+  const int32_t* kv_len;  // may be null
+  uint16_t* out;
+  int* status;
+  int B, H, Tq, Tk, past_len;
+  float scale_log2;
+};
+
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+}  // namespace mla

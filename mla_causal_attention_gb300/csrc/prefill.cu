@@ -1,0 +1,497 @@
+// prefill.cu -- fused causal MLA attention for Tq >= 1 on sm_103a tensor cores.
+//
+// Computes, for every sequence b, head h and query row i (position past_len + i),
+//   out[b,h,i,:] = sum_j softmax_j( scale * [q_nope|q_pe]_i . [k_nope|k_pe_shared]_j ) v_j
+// over the keys j <= i + past_len with j < kv_len[b]: the attention excerpt on the page
+// "Kimi K2 · Similarities" (query/key concat, scores, scale, additive causal mask, fp32
+// softmax, bf16 weights, weighted sum of values), evaluated flash-style so the [Tq, Tk]
+// score matrix never leaves the SM.
+//
+// Work unit (one CTA): one (b, h) and a pair of 128-row query tiles (256 rows).
+// Warp roles (384 threads):
+//   warp 0      TMA producer: both query tiles once, then for every 128-key tile five
+//               16 KB sub-tiles (k_nope cols 0-63, k_nope cols 64-127, the shared
+//               rotary key, v cols 0-63, v cols 64-127) into an 8-slot ring.
+//   warp 1      allocates all 512 TMEM columns; lane 0 issues the MMAs:
+//                 S_t  = Q_t K_j^T     12 x (M128 N128 K16), A and B from shared memory,
+//                                      the 192-wide contraction split 64 | 64 | 64 so the
+//                                      concatenated key is never materialised;
+//                 O_t += P_t V_j       8 x 2 x (M128 N64 K16), P from TMEM, V from smem.
+//               Order per key tile: PV_0(j-1), QK_0(j), PV_1(j-1), QK_1(j), so one
+//               softmax warpgroup works while the tensor core runs the other tile.
+//   warps 4-7   softmax of query tile 0 (thread = row = TMEM lane);
+//   warps 8-11  softmax of query tile 1.  Each reads its S row from TMEM, applies the
+//               causal/padding mask only on tiles that straddle the limit, keeps a
+//               running max (log2 domain) and sum, writes bf16 P over the S columns, and
+//               rescales its O row only when the max grows by more than 2^8 (the stale
+//               max cancels exactly in O / l).  At the end it normalises O and stores
+//               the bf16 row.
+// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512).
+#include <cuda.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "tcgen05.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kBM = 128;       // query rows per tile (TMEM lanes)
+constexpr int kBN = 128;       // keys per tile
+constexpr int kSub = 16384;    // one 128-row x 128-byte (64 bf16) swizzled sub-tile
+constexpr int kSlots = 8;      // K/V ring depth in sub-tiles
+constexpr int kSubPerKv = 5;   // kn0, kn1, kpe, v0, v1
+constexpr int kThreads = 384;
+constexpr int kOffQ = 0;                       // 2 tiles x {nope0, nope1, pe}
+constexpr int kOffRing = kOffQ + 2 * 3 * kSub;  // 98304
+constexpr int kOffBar = kOffRing + kSlots * kSub;  // 229376
+constexpr int kSmemBytes = kOffBar + 256 + 1024;   // barriers + 1 KB alignment slack
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only if max grows > 2^8
+
+struct PrefillParams {
+  CUtensorMap tm_qn;  // q_nope  {128, Tq, B*H}
+  CUtensorMap tm_qr;  // q_pe    {64,  Tq, B*H}
+  CUtensorMap tm_kn;  // k_nope  {128, Tk, B*H}
+  CUtensorMap tm_kr;  // k_pe    {64,  Tk, B}
+  CUtensorMap tm_v;   // v       {128, Tk, B*H}
+  const int32_t* kv_len;
+  uint16_t* out;
+  int* status;
+  int B, H, Tq, Tk, past_len, n_qb;
+  float scale_log2;
+};
+
+struct Bars {
+  uint64_t full[kSlots];
+  uint64_t empty[kSlots];
+  uint64_t q_full;
+  uint64_t s_full[2];
+  uint64_t p_ready[2];
+  uint64_t o_done[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(Bars) <= 256, "barrier block");
+
+__device__ __forceinline__ void setmaxnreg_dec56() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
+}
+__device__ __forceinline__ void setmaxnreg_inc224() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 224;" ::: "memory");
+}
+
+// Keeps the compiler from using tcgen05.ld destinations before tcgen05.wait::ld.
+__device__ __forceinline__ void pin32(uint32_t (&r)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; i += 8)
+    asm volatile("" : "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]),
+                 "+r"(r[i + 4]), "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7]));
+}
+
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(a, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+__device__ __forceinline__ void tma_load_3d_nohint(void* smem_dst, const void* tmap,
+                                                   uint64_t* bar, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    mla_prefill_kernel(const __grid_constant__ PrefillParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  uint8_t* sQ = smem + kOffQ;
+  uint8_t* sRing = smem + kOffRing;
+  Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
+  volatile int* abort_flag = &bars->abort_flag;
+
+  // ---- work unit: heaviest query-tile pairs first ----
+  const int BH = p.B * p.H;
+  const int unit = blockIdx.x;
+  const int qb = p.n_qb - 1 - unit / BH;
+  const int bh = unit % BH;
+  const int b = bh / p.H;
+  const int r0 = qb * 2 * kBM;
+
+  int kvl = p.kv_len ? p.kv_len[b] : p.Tk;
+  if (kvl < 1 || kvl > p.Tk) {
+    if (threadIdx.x == 0) set_status(p.status, MLA_ERR_KVLEN);
+    kvl = min(max(kvl, 1), p.Tk);
+  }
+  int nt[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int rt = r0 + t * kBM;
+    if (rt >= p.Tq) {
+      nt[t] = 0;
+    } else {
+      const int qlast = min(rt + kBM - 1, p.Tq - 1);
+      const int lastkey = min(qlast + p.past_len, kvl - 1);
+      nt[t] = lastkey / kBN + 1;
+    }
+  }
+  const int n = max(nt[0], nt[1]);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(&bars->full[i], 1);
+      mbar_init(&bars->empty[i], 1);
+    }
+    mbar_init(&bars->q_full, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars->s_full[t], 1);
+      mbar_init(&bars->p_ready[t], 4);
+      mbar_init(&bars->o_done[t], 1);
+    }
+    mbar_init(&bars->mma_done, 1);
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&bars->tmem_base, 512);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tbase = bars->tmem_base;
+
+  if (warp < 4) {
+    setmaxnreg_dec56();
+    if (warp == 0 && lane == 0) {
+      // ================= TMA producer =================
+      prefetch_tmap(&p.tm_qn);
+      prefetch_tmap(&p.tm_qr);
+      prefetch_tmap(&p.tm_kn);
+      prefetch_tmap(&p.tm_kr);
+      prefetch_tmap(&p.tm_v);
+      const uint64_t pol_q = l2_policy_evict_first();
+      const uint32_t qbytes = (uint32_t)((nt[0] > 0 ? 3 : 0) + (nt[1] > 0 ? 3 : 0)) * kSub;
+      mbar_arrive_expect_tx(&bars->q_full, qbytes);
+      for (int t = 0; t < 2; ++t) {
+        if (nt[t] == 0) continue;
+        const int rt = r0 + t * kBM;
+        tma_load_3d(sQ + (t * 3 + 0) * kSub, &p.tm_qn, &bars->q_full, 0, rt, bh, pol_q);
+        tma_load_3d(sQ + (t * 3 + 1) * kSub, &p.tm_qn, &bars->q_full, 64, rt, bh, pol_q);
+        tma_load_3d(sQ + (t * 3 + 2) * kSub, &p.tm_qr, &bars->q_full, 0, rt, bh, pol_q);
+      }
+      int u = 0;
+      bool ok = true;
+      for (int j = 0; j < n && ok; ++j) {
+        const int jt = j * kBN;
+        for (int s = 0; s < kSubPerKv; ++s, ++u) {
+          const int slot = u % kSlots;
+          if (u >= kSlots &&
+              !mbar_wait(&bars->empty[slot], ((u / kSlots) - 1) & 1, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* dst = sRing + slot * kSub;
+          uint64_t* fb = &bars->full[slot];
+          mbar_arrive_expect_tx(fb, kSub);
+          switch (s) {
+            case 0: tma_load_3d_nohint(dst, &p.tm_kn, fb, 0, jt, bh); break;
+            case 1: tma_load_3d_nohint(dst, &p.tm_kn, fb, 64, jt, bh); break;
+            case 2: tma_load_3d_nohint(dst, &p.tm_kr, fb, 0, jt, b); break;
+            case 3: tma_load_3d_nohint(dst, &p.tm_v, fb, 0, jt, bh); break;
+            default: tma_load_3d_nohint(dst, &p.tm_v, fb, 64, jt, bh); break;
+          }
+        }
+      }
+      // Every load this thread issued must land before shared memory is released.
+      drain_wait(&bars->q_full, 0);
+      for (int v = max(0, u - kSlots); v < u; ++v) drain_wait(&bars->full[v % kSlots], (v / kSlots) & 1);
+    } else if (warp == 1 && lane == 0) {
+      // ================= MMA issuer =================
+      constexpr uint32_t kIdescQK = tc::idesc_bf16_f32(128, 128, false);
+      constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(128, 64, true);
+      bool ok = mbar_wait(&bars->q_full, 0, p.status, abort_flag);
+      tc::fence_after_sync();
+      const uint32_t q_addr = smem_u32(sQ);
+      const uint32_t ring_addr = smem_u32(sRing);
+      for (int j = 0; j <= n && ok; ++j) {
+        const int uk = j * kSubPerKv;         // first sub-tile of K(j)
+        const int uv = (j - 1) * kSubPerKv + 3;  // first sub-tile of V(j-1)
+        if (j < n) {
+          for (int s = 0; s < 3 && ok; ++s)
+            ok = mbar_wait(&bars->full[(uk + s) % kSlots], ((uk + s) / kSlots) & 1, p.status,
+                           abort_flag);
+        }
+        if (j > 0) {
+          for (int s = 0; s < 2 && ok; ++s)
+            ok = mbar_wait(&bars->full[(uv + s) % kSlots], ((uv + s) / kSlots) & 1, p.status,
+                           abort_flag);
+        }
+        if (!ok) break;
+        tc::fence_after_sync();
+#pragma unroll 1
+        for (int t = 0; t < 2; ++t) {
+          const uint32_t s_tmem = tbase + t * 128;
+          const uint32_t o_tmem = tbase + 256 + t * 128;
+          if (j > 0 && j - 1 < nt[t]) {
+            // O_t += P_t(j-1) V(j-1): P from TMEM (aliasing S_t), V MN-major from smem.
+            if (!mbar_wait(&bars->p_ready[t], (j - 1) & 1, p.status, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc::fence_after_sync();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+#pragma unroll
+              for (int hf = 0; hf < 2; ++hf) {
+                const uint32_t vaddr = ring_addr + ((uv + hf) % kSlots) * kSub + kk * 2048;
+                const uint64_t bdesc = tc::smem_desc_sw128(vaddr, 16, 1024);
+                tc::mma_ts(o_tmem + hf * 64, s_tmem + kk * 8, bdesc, kIdescPV,
+                           (j - 1 > 0 || kk > 0) ? 1u : 0u);
+              }
+            }
+            if (j - 1 == nt[t] - 1) tc::commit(&bars->o_done[t]);
+          }
+          if (t == 1 && j > 0) {
+            // V(j-1) is no longer needed once both value mixes have run.
+            tc::commit(&bars->empty[uv % kSlots]);
+            tc::commit(&bars->empty[(uv + 1) % kSlots]);
+          }
+          if (j < nt[t]) {
+            // S_t = Q_t K(j)^T over 192 columns: 4 k-steps per 64-column sub-tile.
+            const uint32_t qa = q_addr + t * 3 * kSub;
+#pragma unroll
+            for (int kk = 0; kk < 12; ++kk) {
+              const int sub = kk >> 2;
+              const uint32_t koff = (kk & 3) * 32;
+              const uint64_t adesc = tc::smem_desc_sw128(qa + sub * kSub + koff, 16, 1024);
+              const uint32_t kaddr = ring_addr + ((uk + sub) % kSlots) * kSub + koff;
+              const uint64_t bdesc = tc::smem_desc_sw128(kaddr, 16, 1024);
+              tc::mma_ss(s_tmem, adesc, bdesc, kIdescQK, kk > 0 ? 1u : 0u);
+            }
+            tc::commit(&bars->s_full[t]);
+          }
+        }
+        if (j < n && ok) {
+          for (int s = 0; s < 3; ++s) tc::commit(&bars->empty[(uk + s) % kSlots]);
+        }
+      }
+      // No MMA may still be running when TMEM is released.
+      tc::commit(&bars->mma_done);
+      drain_wait(&bars->mma_done, 0);
+    }
+    __syncwarp();
+  } else {
+    // ================= softmax warpgroups =================
+    setmaxnreg_inc224();
+    const int t = (warp >> 2) - 1;  // query tile 0 or 1
+    const int tw = threadIdx.x - 128 * (t + 1);
+    const int qi = r0 + t * kBM + tw;  // query row within the sequence
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t s_tmem = tbase + lane_off + t * 128;
+    const uint32_t o_tmem = tbase + lane_off + 256 + t * 128;
+    const int limit = min(qi + p.past_len + 1, kvl);  // keys [0, limit) are visible
+    const float sl2 = p.scale_log2;
+    float m = -INFINITY;
+    float l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nt[t]; ++j) {
+      if (!mbar_wait(&bars->s_full[t], j & 1, p.status, abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+      uint32_t r[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tc::tmem_ld32(s_tmem + c * 32, r[c]);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) pin32(r[c]);
+
+      const int jt = j * kBN;
+      if (jt + kBN > limit) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            if (jt + c * 32 + e >= limit) r[c][e] = __float_as_uint(-INFINITY);
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(r[c][e]));
+      const float m_tile = mx * sl2;
+      if (j == 0) {
+        m = m_tile;
+      } else {
+        const bool need = m_tile > m + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+          const float alpha = need ? ex2_approx(m - m_tile) : 1.0f;
+          if (need) {
+            m = m_tile;
+            l *= alpha;
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tc::tmem_ld32(o_tmem + c * 32, o);
+            tc::tmem_wait_ld();
+            pin32(o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tc::tmem_st32(o_tmem + c * 32, o);
+          }
+        }
+      }
+      const float neg_m = -m;
+      float sum0 = 0.f, sum1 = 0.f;
+      uint32_t pk[2][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          const float x0 = ex2_approx(fmaf(__uint_as_float(r[c][e]), sl2, neg_m));
+          const float x1 = ex2_approx(fmaf(__uint_as_float(r[c][e + 1]), sl2, neg_m));
+          sum0 += x0;
+          sum1 += x1;
+          pk[c >> 1][(c & 1) * 16 + (e >> 1)] = pack_bf16x2(x0, x1);
+        }
+      }
+      l += sum0 + sum1;
+      tc::tmem_st32(s_tmem, pk[0]);
+      tc::tmem_st32(s_tmem + 32, pk[1]);
+      tc::tmem_wait_st();
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->p_ready[t]);
+    }
+    if (ok && nt[t] > 0) {
+      if (mbar_wait(&bars->o_done[t], 0, p.status, abort_flag)) {
+        tc::fence_after_sync();
+        uint32_t o[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tc::tmem_ld32(o_tmem + c * 32, o[c]);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) pin32(o[c]);
+        const float inv = 1.0f / l;
+        if (qi < p.Tq) {
+          uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)bh * p.Tq + qi) * 128);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(o[c][v * 8 + 0]) * inv,
+                                __uint_as_float(o[c][v * 8 + 1]) * inv);
+              w.y = pack_bf16x2(__uint_as_float(o[c][v * 8 + 2]) * inv,
+                                __uint_as_float(o[c][v * 8 + 3]) * inv);
+              w.z = pack_bf16x2(__uint_as_float(o[c][v * 8 + 4]) * inv,
+                                __uint_as_float(o[c][v * 8 + 5]) * inv);
+              w.w = pack_bf16x2(__uint_as_float(o[c][v * 8 + 6]) * inv,
+                                __uint_as_float(o[c][v * 8 + 7]) * inv);
+              dst[c * 4 + v] = w;
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tbase, 512);
+  }
+}
+
+// ---- host side: tensor maps and launch -------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// bf16 tensor viewed as {inner, rows, planes} with 128-byte swizzled {64, 128, 1} boxes;
+// rows past the end of a plane read as zeros.
+bool encode_3d(EncodeTiledFn fn, CUtensorMap* m, const void* base, uint64_t inner,
+               uint64_t rows, uint64_t planes) {
+  cuuint64_t dims[3] = {inner, rows, planes};
+  cuuint64_t strides[2] = {inner * 2, inner * 2 * rows};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  PrefillParams p;
+  const uint64_t BH = (uint64_t)a.B * a.H;
+  if (!encode_3d(fn, &p.tm_qn, a.q_nope, 128, a.Tq, BH) ||
+      !encode_3d(fn, &p.tm_qr, a.q_pe, 64, a.Tq, BH) ||
+      !encode_3d(fn, &p.tm_kn, a.k_nope, 128, a.Tk, BH) ||
+      !encode_3d(fn, &p.tm_kr, a.k_pe, 64, a.Tk, a.B) ||
+      !encode_3d(fn, &p.tm_v, a.v, 128, a.Tk, BH))
+    return cudaErrorInvalidValue;
+  p.kv_len = a.kv_len;
+  p.out = a.out;
+  p.status = a.status;
+  p.B = a.B;
+  p.H = a.H;
+  p.Tq = a.Tq;
+  p.Tk = a.Tk;
+  p.past_len = a.past_len;
+  p.n_qb = (a.Tq + 2 * kBM - 1) / (2 * kBM);
+  p.scale_log2 = a.scale_log2;
+  const uint64_t units = BH * (uint64_t)p.n_qb;
+  if (units > 0x7fffffffull) return cudaErrorInvalidValue;
+
+  static int attr_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (attr_device != dev) {
+    e = cudaFuncSetAttribute(mla_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_device = dev;
+  }
+  mla_prefill_kernel<<<(unsigned)units, kThreads, kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -1,0 +1,109 @@
+"""Prefill path (tcgen05 / TMEM / TMA kernel) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+from mla_causal_attention_gb300.binding import PATH_PREFILL
+from mla_causal_attention_gb300.inputs import make_inputs
+from mla_causal_attention_gb300.workloads import WORKLOADS, Workload, softmax_scale_192
+from gpu_helpers import assert_close, gpu_rows, oracle_for, run_gpu, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def wl(B, H, Tq, past, kv=None, vs=1.0):
+    return Workload("t", B, H, Tq, past, vs, kv, softmax_scale_192())
+
+
+def test_tiny_prefill_full():
+    inp = make_inputs(WORKLOADS["tiny_prefill"], seed=0)
+    out = run_gpu(to_device(inp))
+    assert_close(gpu_rows(out), oracle_for(inp), "tiny_prefill")
+
+
+@pytest.mark.parametrize("B,H,Tq,past,kv", [
+    (1, 2, 1, 0, None),        # one query through the prefill path
+    (1, 2, 2, 0, None),
+    (2, 3, 17, 0, None),
+    (1, 2, 129, 0, None),      # one row past a tile
+    (1, 2, 255, 5, None),
+    (1, 2, 256, 0, None),      # exactly one tile pair
+    (1, 2, 257, 3, None),      # ragged second pair
+    (2, 2, 300, 77, (200, 377)),  # padding inside the causal range, unaligned past_len
+    (1, 4, 512, 1000, None),   # many key tiles before the diagonal
+    (3, 2, 130, 126, (5, 256)),
+])
+def test_prefill_shapes_full(B, H, Tq, past, kv):
+    inp = make_inputs(wl(B, H, Tq, past, kv), seed=5)
+    out = run_gpu(to_device(inp), path=PATH_PREFILL)
+    assert_close(gpu_rows(out), oracle_for(inp), f"prefill B{B} H{H} Tq{Tq} past{past}")
+
+
+def test_chunked_prefill_small_full():
+    inp = make_inputs(wl(2, 4, 384, 640, (900, 1024)), seed=6)
+    out = run_gpu(to_device(inp))
+    assert_close(gpu_rows(out), oracle_for(inp), "chunked small")
+
+
+def _sample_rows(w, heads, qs):
+    return [(b * w.H + h) * w.Tq + i for b in range(w.B) for h in heads for i in qs]
+
+
+def test_long_prefill_full_size_sampled():
+    w = WORKLOADS["long_prefill"]
+    inp = make_inputs(w, seed=0)
+    out = run_gpu(to_device(inp))
+    rng = np.random.default_rng(0)
+    qs = sorted({0, 1, 127, 128, 255, 256, 1000, 2047, 2048, 4094, 4095,
+                 *rng.integers(0, w.Tq, 12).tolist()})
+    rows = _sample_rows(w, [0, 1, 31, 63], qs)
+    assert_close(gpu_rows(out, rows), oracle_for(inp, rows), "long_prefill sampled")
+
+
+def test_chunked_prefill_full_size_sampled():
+    w = WORKLOADS["chunked_prefill"]
+    inp = make_inputs(w, seed=0)
+    out = run_gpu(to_device(inp))
+    rng = np.random.default_rng(1)
+    qs = sorted({0, 1, 255, 256, 1023, 2046, 2047, *rng.integers(0, w.Tq, 6).tolist()})
+    rows = _sample_rows(w, [0, 40, 63], qs)
+    assert_close(gpu_rows(out, rows), oracle_for(inp, rows), "chunked_prefill sampled")
+
+
+def test_prefill_first_row_is_exact():
+    inp = make_inputs(wl(2, 3, 200, 0), seed=7)
+    out = run_gpu(to_device(inp)).cpu()
+    assert torch.equal(out[:, :, 0, :], inp["v"][:, :, 0, :])
+
+
+def test_prefill_hidden_keys_do_not_matter():
+    w = wl(2, 2, 300, 100, (250, 400))
+    inp = make_inputs(w, seed=8)
+    base = run_gpu(to_device(inp)).cpu()
+    for b in range(2):
+        k = int(inp["kv_len"][b])
+        inp["k_nope"][b, :, k:] = 1e30
+        inp["k_pe_shared"][b, k:] = -1e30
+        inp["v"][b, :, k:] = 1e30
+    again = run_gpu(to_device(inp)).cpu()
+    assert torch.equal(base, again)
+    # causal part: keys after the last query's position never matter for row 0..9
+    inp2 = make_inputs(wl(1, 2, 260, 0), seed=9)
+    ref = run_gpu(to_device(inp2)).cpu()
+    inp2["k_nope"][0, :, 10:] = 1e30
+    inp2["v"][0, :, 10:] = -1e30
+    inp2["k_pe_shared"][0, 10:] = 1e30
+    out = run_gpu(to_device(inp2)).cpu()
+    assert torch.equal(out[0, :, :10], ref[0, :, :10])
+
+
+def test_prefill_equal_scores_give_mean():
+    w = wl(1, 2, 300, 40)
+    inp = make_inputs(w, seed=10)
+    inp["q_nope"].zero_()
+    inp["q_pe"].zero_()
+    out = run_gpu(to_device(inp)).double().cpu()
+    v = inp["v"].double()
+    for i in (0, 1, 100, 299):
+        want = v[0, :, : i + 41].mean(dim=1)
+        assert (out[0, :, i] - want).abs().max() < 8e-3
