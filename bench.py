@@ -1,0 +1,494 @@
+#!/usr/bin/env python
+"""Benchmark of the MLA causal-attention library on GB300.
+
+One JSON line per run (rank 0).  The headline workload is the long causal prefill
+(B=1, H=64, Tq=Tk=4096, dims 192/128, k_pe shared, inputs N(0,1)*0.5) measured in
+TFLOP/s of visible (query, key) pairs; the batched ragged decode (B=64, H=64,
+kv_len ~ U[512, 8192]) is reported in the same line under "secondary" in GB/s of
+algorithmic HBM bytes.  Every step is one call of the library's C ABI on inputs already
+resident in device memory; L2 is flushed (a 2x-L2 write) before every timed step, outside
+the step's CUDA events.  "e2e" repeats the measurement through the public API from pinned
+host buffers, host->device copies and the device->host read of the output included.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--secondary NAME|none]
+
+--impl reference times the fp64 CPU oracle (the correctness reference, run as it stands)
+on the host cores on a bounded sample of the same workload.  Under torchrun each rank
+runs its own replica of the workload on its own GPU (the path has no cross-GPU step);
+value = all ranks' work / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="long_prefill")
+    ap.add_argument("--secondary", default="decode_ragged")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the workload's batch size (profiling of smaller cases)")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------------------
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            return d, "measured"
+        except Exception:
+            pass
+    return {}, "fallback"
+
+
+def peak_for(kind: str, sustained: bool):
+    d, src = measured_peaks()
+    if kind == "hbm":
+        for k in ("hbm_gbs", "hbm_GBps", "hbm"):
+            if isinstance(d.get(k), (int, float)):
+                return float(d[k]), f"{src} hbm_gbs"
+        return FALLBACK_HBM_GBS, "fallback 6.8 TB/s"
+    keys = ("bf16_tflops_sustained", "bf16_tflops") if sustained else ("bf16_tflops",)
+    for k in keys:
+        if isinstance(d.get(k), (int, float)):
+            return float(d[k]), f"{src} {k}"
+    return FALLBACK_BF16_TFLOPS, "fallback 1.9 PFLOP/s bf16"
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mla_causal_attention_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode())
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches this source."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[kernel]
+        if e.get("source_sha256") != kernel_source_sha():
+            return None
+        return int(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"mla_bench_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 7:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    mx.append(float(parts[1]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[3:7]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        except OSError:
+            return None
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The slowest rank's time: every rank gets the same value (all-reduce MAX)."""
+    if world <= 1:
+        return float(x)
+    import torch
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(work_per_rank: int, world: int, max_ms: float, scale: float) -> float:
+    """Units processed by all ranks (each rank its own equal-size replica) / slowest time."""
+    return work_per_rank * world / (max_ms * 1e-3) * scale
+
+
+# ---------------------------------------------------------------------------------------
+def workload_metrics(wl, kv_len):
+    from mla_causal_attention_gb300.workloads import algorithmic_bytes, algorithmic_flops
+
+    if wl.Tq == 1:
+        return {"kind": "decode", "unit": "GB/s", "work": algorithmic_bytes(wl, kv_len),
+                "scale": 1e-9, "bound": "hbm", "roof_unit": "GB/s"}
+    return {"kind": "prefill", "unit": "TFLOP/s", "work": algorithmic_flops(wl, kv_len),
+            "scale": 1e-12, "bound": "tensor", "roof_unit": "TFLOP/s"}
+
+
+def launches_per_call(wl):
+    if wl.Tq > 1:
+        return 1
+    from mla_causal_attention_gb300.binding import decode_plan
+
+    _, splits = decode_plan(wl.B, wl.H, wl.Tk)
+    return 1 if splits == 1 else 2
+
+
+def measure_ours(wl, args, rank, world, local, with_cpu):
+    import numpy as np
+    import torch
+
+    from mla_causal_attention_gb300 import binding
+    from mla_causal_attention_gb300.inputs import make_inputs
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    host = make_inputs(wl, seed=args.seed + rank, pin_memory=True)
+    keys = ("q_nope", "q_pe", "k_nope", "k_pe_shared", "v", "kv_len")
+    d = {k: host[k].to(dev) for k in keys}
+    out = torch.empty((wl.B, wl.H, wl.Tq, 128), dtype=torch.bfloat16, device=dev)
+    ws = binding.Workspace(dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    m = workload_metrics(wl, host["kv_len"].numpy())
+
+    def call():
+        binding.mla_attn_fwd(d["q_nope"], d["q_pe"], d["k_nope"], d["k_pe_shared"], d["v"],
+                             d["kv_len"], wl.past_len, wl.softmax_scale, out=out,
+                             workspace=ws, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize()
+    if binding.mla_attn_get_status(ws, dev) != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    barrier()
+    wall0 = time.perf_counter()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)  # evicts L2 outside the step's events
+            starts[i].record(stream)
+            call()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    barrier()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
+    st = binding.mla_attn_get_status(ws, dev)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after timed region")
+    ms = total_ms / args.steps
+    value = whole_job_rate(m["work"], world, ms, m["scale"])
+    per_launch_ms = ms  # one call = the launches of this path, timed together
+    bf16_sustained = args.steps * ms > 2000.0
+    if m["bound"] == "hbm":
+        peak, peak_src = peak_for("hbm", False)
+    else:
+        peak, peak_src = peak_for("tensor", bf16_sustained)
+    achieved = m["work"] / (per_launch_ms * 1e-3) * m["scale"]
+    kernel_name = "mla_prefill_kernel" if m["kind"] == "prefill" else "decode_splitkv_kernel"
+    traffic = recorded_traffic(kernel_name)
+    res = {
+        "value": value, "unit": m["unit"], "ms_per_step": ms,
+        "step_ms_min": min(step_ms), "step_ms_max": max(step_ms),
+        "wall_s_timed_region": wall,
+        "roofline": {"bound": m["bound"], "achieved": achieved, "peak": peak,
+                     "unit": m["roof_unit"], "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": peak_src, "kernel": kernel_name,
+                     "algorithmic_per_launch": m["work"]},
+        "clocks": clk.summary(),
+        "gpu_launches": launches_per_call(wl) * args.steps,
+        "work_per_step": m["work"],
+    }
+
+    if not args.no_e2e:
+        res["e2e"] = measure_e2e(wl, host, d, out, ws, stream, m, args, world)
+    if with_cpu and rank == 0 and world == 1:
+        res["cpu_baseline"] = cpu_baseline(wl, host, m, args.cpu_seconds)
+    del flush
+    return res
+
+
+def measure_e2e(wl, host, d, out, ws, stream, m, args, world):
+    """Same metric through the public API from pinned host memory, copies included."""
+    import torch
+
+    from mla_causal_attention_gb300 import binding
+
+    keys = ("q_nope", "q_pe", "k_nope", "k_pe_shared", "v", "kv_len")
+    out_host = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(host[k].numel() * host[k].element_size() for k in keys)
+    d2h = out.numel() * out.element_size()
+    steps = max(1, min(args.steps, 10))
+
+    def step():
+        for k in keys:
+            d[k].copy_(host[k], non_blocking=True)
+        binding.mla_attn_fwd(d["q_nope"], d["q_pe"], d["k_nope"], d["k_pe_shared"], d["v"],
+                             d["kv_len"], wl.past_len, wl.softmax_scale, out=out,
+                             workspace=ws, stream=stream)
+        out_host.copy_(out, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1) / steps, world, out.device)
+    return {"value": whole_job_rate(m["work"], world, ms, m["scale"]), "unit": m["unit"],
+            "ms_per_step": ms, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "steps": steps}
+
+
+# ---------------------------------------------------------------------------------------
+def _sample_rows(wl, kv_len, n, rng):
+    """n random output rows (flat (b*H + h)*Tq + i) and their algorithmic work."""
+    import numpy as np
+
+    rows = rng.integers(0, wl.B * wl.H * wl.Tq, size=n)
+    i = rows % wl.Tq
+    b = rows // (wl.H * wl.Tq)
+    kv = np.asarray(kv_len, dtype=np.int64)[b]
+    vis = np.minimum(i + wl.past_len + 1, kv)
+    if wl.Tq > 1:
+        work = 640 * int(vis.sum())
+    else:  # bytes the row reads: its K/V rows, its share of the rotary key, q and out
+        work = int((vis * (512 + 128 / wl.H)).sum() + n * 768)
+    return rows, work
+
+
+def cpu_baseline(wl, host, m, target_s):
+    """The oracle, as it stands, on a bounded random sample of the workload's rows."""
+    import numpy as np
+
+    from oracle import oracle_rows
+
+    threads = len(os.sched_getaffinity(0))
+    rng = np.random.default_rng(1234)
+    args = (host["q_nope"], host["q_pe"], host["k_nope"], host["k_pe_shared"], host["v"],
+            host["kv_len"], wl.past_len, wl.softmax_scale)
+    n = max(threads, 8)
+    rows, work = _sample_rows(wl, host["kv_len"].numpy(), n, rng)
+    t0 = time.perf_counter()
+    oracle_rows(*args, rows=rows, threads=threads)
+    dt = time.perf_counter() - t0
+    rate = work / max(dt, 1e-6)
+    # grow the sample to about target_s seconds of oracle work
+    want = int(n * min(max(target_s / max(dt, 1e-6), 1.0), 1e6))
+    want = min(want, wl.B * wl.H * wl.Tq)
+    if want > n:
+        rows, work = _sample_rows(wl, host["kv_len"].numpy(), want, rng)
+        t0 = time.perf_counter()
+        oracle_rows(*args, rows=rows, threads=threads)
+        dt = time.perf_counter() - t0
+        rate = work / dt
+    return {"value": rate * m["scale"], "unit": m["unit"], "cores": threads, "kind": "oracle",
+            "sample": f"{len(rows)} random output rows of {wl.name} (full key range each), "
+                      f"{dt:.1f} s on {threads} threads", "seconds": dt}
+
+
+def run_reference(args, wl):
+    """--impl reference: the fp64 CPU oracle on the host cores, a bounded sample per step."""
+    import numpy as np
+
+    from mla_causal_attention_gb300.inputs import draw_kv_len, make_inputs
+    from oracle import oracle_rows
+
+    sub = wl.with_(B=1) if wl.B > 1 else wl
+    host = make_inputs(wl, seed=args.seed, batches=[0])
+    m = workload_metrics(wl, draw_kv_len(wl, args.seed).numpy())
+    threads = len(os.sched_getaffinity(0))
+    kv = host["kv_len"].numpy()
+    rng = np.random.default_rng(99)
+    a = (host["q_nope"], host["q_pe"], host["k_nope"], host["k_pe_shared"], host["v"],
+         host["kv_len"], sub.past_len, sub.softmax_scale)
+    # calibrate a per-step sample of about 2 s
+    n = max(threads, 8)
+    rows, work = _sample_rows(sub, kv, n, rng)
+    t0 = time.perf_counter()
+    oracle_rows(*a, rows=rows, threads=threads)
+    dt = time.perf_counter() - t0
+    n = max(n, min(int(n * 2.0 / max(dt, 1e-6)), sub.B * sub.H * sub.Tq))
+    for _ in range(args.warmup):
+        rows, work = _sample_rows(sub, kv, min(n, 64), rng)
+        oracle_rows(*a, rows=rows, threads=threads)
+    total_work, total_s = 0, 0.0
+    for _ in range(args.steps):
+        rows, work = _sample_rows(sub, kv, n, rng)
+        t0 = time.perf_counter()
+        oracle_rows(*a, rows=rows, threads=threads)
+        total_s += time.perf_counter() - t0
+        total_work += work
+    value = total_work / total_s * m["scale"]
+    line = base_line(args, wl, m, value, total_s / args.steps * 1e3)
+    line.update({
+        "impl": "reference",
+        "dtype": "f64",
+        "cpu_baseline": {"value": value, "unit": m["unit"], "cores": threads, "kind": "oracle",
+                         "sample": f"{n} random output rows of {wl.name} per step (sequence 0)"},
+        "e2e": {"value": value, "unit": m["unit"], "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    })
+    print(json.dumps(line))
+
+
+def base_line(args, wl, m, value, ms):
+    metric = "prefill causal attn TFLOP/s & decode KV-read GB/s, % of GB300 roofline"
+    return {
+        "metric": metric, "value": value, "unit": m["unit"], "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 inputs; no weights needed)",
+        "config": workload_config(wl, args),
+    }
+
+
+def workload_config(wl, args):
+    return {"workload": wl.name, "B": wl.B, "H": wl.H, "Tq": wl.Tq, "Tk": wl.Tk,
+            "past_len": wl.past_len, "kv_len_range": wl.kv_len_range,
+            "value_scale": wl.value_scale, "head_dims": "qk 128+64 (k_pe shared), v 128",
+            "softmax_scale": wl.softmax_scale, "seed": args.seed,
+            "l2": "flushed (2x L2 write) before every timed step, outside its events",
+            "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    from mla_causal_attention_gb300.workloads import WORKLOADS
+
+    wl = WORKLOADS[args.workload]
+    if args.batch:
+        wl = wl.with_(B=args.batch, name=f"{wl.name}_b{args.batch}")
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, wl)
+        return 0
+
+    import torch
+
+    from mla_causal_attention_gb300.build import build_library
+
+    if rank == 0:
+        build_library()
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
+        build_library()
+    res = measure_ours(wl, args, rank, world, local, with_cpu=not args.no_cpu)
+    sec = None
+    if args.secondary and args.secondary != "none" and args.secondary != args.workload:
+        swl = WORKLOADS[args.secondary]
+        sec = measure_ours(swl, args, rank, world, local, with_cpu=not args.no_cpu)
+        sec["config"] = workload_config(swl, args)
+    if rank == 0:
+        m = workload_metrics(wl, [wl.Tk] * wl.B)
+        line = base_line(args, wl, m, res["value"], res["ms_per_step"])
+        line["impl"] = "ours"
+        for k in ("roofline", "cpu_baseline", "e2e", "clocks", "gpu_launches"):
+            if k in res:
+                line[k] = res[k]
+        line["step_ms_min"] = res["step_ms_min"]
+        line["step_ms_max"] = res["step_ms_max"]
+        if sec is not None:
+            line["secondary"] = [{"workload": args.secondary, **{k: v for k, v in sec.items()
+                                                                if k != "work_per_step"}}]
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

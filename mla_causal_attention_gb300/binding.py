@@ -157,7 +157,9 @@ def mla_attn_fwd(q_nope, q_pe, k_nope, k_pe_shared, v, kv_len, past_len: int,
     _check(out, "out", bf, (B, H, Tq, 128), dev)
     ws_bytes = lib.mla_attn_workspace_bytes(B, H, Tq, Tk)
     if decode_chunk:
-        ws_bytes = max(ws_bytes, 256 + B * H * (-(-Tk // decode_chunk)) * 130 * 4)
+        splits = -(-Tk // decode_chunk)
+        ws_bytes = max(ws_bytes, 256 + (-(-B * H * splits * 8 // 256)) * 256
+                       + B * H * splits * 512)
     ws = (workspace or _default_workspace(dev)).get(ws_bytes)
     s = stream if stream is not None else torch.cuda.current_stream(dev)
     handle = ctypes.c_void_p(s.cuda_stream)

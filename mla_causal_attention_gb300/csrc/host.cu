@@ -68,9 +68,17 @@ void plan_decode(int B, int H, int Tk, int sms, int* chunk, int* splits) {
   *splits = (Tk + c - 1) / c;
 }
 
+// Partials: (max, sum) pairs, then the 128-float accumulators starting on a 256-byte
+// boundary (the kernels access them with 16-byte vector loads and stores).
+size_t decode_ml_bytes(int B, int H, int splits) {
+  const size_t raw = (size_t)B * H * splits * 2 * sizeof(float);
+  return (raw + 255) & ~(size_t)255;
+}
+
 size_t decode_workspace(int B, int H, int splits) {
   if (splits <= 1) return kStatusBytes;
-  return kStatusBytes + (size_t)B * H * splits * (2 + 128) * sizeof(float);
+  return kStatusBytes + decode_ml_bytes(B, H, splits) +
+         (size_t)B * H * splits * 128 * sizeof(float);
 }
 
 }  // namespace
@@ -163,9 +171,9 @@ mla_status mla_attn_fwd_ex(const uint16_t* q_nope, const uint16_t* q_pe,
     DecodeArgs a;
     a.q_nope = q_nope; a.q_pe = q_pe; a.k_nope = k_nope; a.k_pe = k_pe_shared; a.v = v;
     a.kv_len = kv_len; a.out = out; a.status = status;
-    float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + kStatusBytes);
-    a.part_ml = part;
-    a.part_acc = part + (size_t)B * H * splits * 2;
+    uint8_t* part = static_cast<uint8_t*>(workspace) + kStatusBytes;
+    a.part_ml = reinterpret_cast<float*>(part);
+    a.part_acc = reinterpret_cast<float*>(part + decode_ml_bytes(B, H, splits));
     a.B = B; a.H = H; a.Tk = Tk; a.chunk = chunk; a.splits = splits;
     a.scale_log2 = scale_log2;
     return launch_decode(a, stream) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;

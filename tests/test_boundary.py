@@ -49,8 +49,18 @@ def test_workspace_sizes(lib):
     # decode: status word + per-(b, h, split) (max, sum, 128 accumulators) in fp32
     c, s = binding.decode_plan(64, 64, 8192)
     assert c % 64 == 0 and s == -(-8192 // c)
-    want = 256 if s == 1 else 256 + 64 * 64 * s * 130 * 4
+    ml = -(-(64 * 64 * s * 8) // 256) * 256
+    want = 256 if s == 1 else 256 + ml + 64 * 64 * s * 128 * 4
     assert binding.mla_attn_workspace_bytes(64, 64, 1, 8192) == want
+
+
+def test_workspace_keeps_accumulators_16_byte_aligned(lib):
+    # an odd number of (b, h, split) partials must not misalign the accumulator array
+    for B, H, Tk in [(1, 1, 200), (3, 5, 77), (1, 3, 1000)]:
+        c, s = binding.decode_plan(B, H, Tk)
+        n = binding.mla_attn_workspace_bytes(B, H, 1, Tk)
+        if s > 1:
+            assert (n - 256 - B * H * s * 512) % 256 == 0
 
 
 def test_decode_plan_is_sane(lib):
