@@ -143,6 +143,31 @@ MLA_API const char* mla_status_string(mla_status status);
  */
 MLA_API mla_status mla_attn_decode_plan(int B, int H, int Tk, int* chunk, int* splits);
 
+/*
+ * Decode (Tq == 1, past_len = Tk - 1) without a caller-provided workspace.  The pages
+ * have no counterpart to this call: it exists for callers that cannot allocate device
+ * memory for the library (a server whose KV-cache pool owns all free HBM, a plugin inside
+ * a framework whose allocator owns the device, a loop that cannot afford cudaMalloc's
+ * implicit synchronisation).  The split-KV partials live in a 32 MiB array inside the
+ * library image, which every GPU that loads the library holds until the process exits.
+ *
+ * Arguments and result are those of mla_attn_fwd with Tq = 1 and the same split plan, so
+ * the output matches mla_attn_fwd's.  device_status (device int, may be NULL) receives
+ * device-detected errors (MLA_ERR_KVLEN) the way the workspace status word does; the
+ * caller zeroes and reads it.  Returns MLA_ERR_WORKSPACE when the plan for these sizes
+ * needs more than the 32 MiB array (B * H * splits partials of 520 bytes each).
+ *
+ * The call allocates nothing.  Its first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture.  All calls share the array: calls that overlap on the GPU (other
+ * streams, other host threads) race on it and must be serialised by the caller.
+ */
+MLA_API mla_status mla_attn_decode_noalloc(const uint16_t* q_nope, const uint16_t* q_pe,
+                                           const uint16_t* k_nope, const uint16_t* k_pe_shared,
+                                           const uint16_t* v, const int32_t* kv_len, int B,
+                                           int H, int Tk, float softmax_scale, uint16_t* out,
+                                           int* device_status, void* cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif
