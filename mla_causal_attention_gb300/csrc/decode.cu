@@ -10,7 +10,7 @@
 // streams each 32-key stage with 1-D bulk copies into a 3-deep shared-memory ring: the
 // shared rotary-key rows once per stage, then the no-rope key and value rows of the four
 // heads.  Two consumer warps per head split the stage's keys: 8 lanes per key form the
-// 192-wide dot product (128-bit shared loads, 3 shuffles), the warp keeps a running
+// 192-wide dot product (conflict-free 128-bit shared loads, 3 shuffles), the warp keeps a running
 // (max, sum) in the log2 domain, and every lane accumulates 4 output columns.  The CTA
 // writes either the final bf16 row (single split) or a (max, sum, acc[128]) partial that
 // the combine kernel merges:  m = max m_s,  l = sum 2^(m_s - m) l_s,
@@ -159,13 +159,15 @@ __global__ void __launch_bounds__(DecCfg<G, T, NST, WPH>::kThreads, 1)
   const int tk = lane >> 3;
   const size_t bh = (size_t)b * p.H + h0 + (head_ok ? g : 0);
 
-  // This lane's slice of the query, pre-multiplied by softmax_scale * log2(e): 16 of the
-  // 128 no-rope columns and 8 of the 64 rotary columns.
+  // This lane's slice of the query, pre-multiplied by softmax_scale * log2(e): no-rope
+  // columns [8*l8, 8*l8+8) and [64+8*l8, 64+8*l8+8), rotary columns [8*l8, 8*l8+8).  With
+  // this split the 8 lanes of a key read each 128-byte half-row of shared memory once,
+  // so the 4 keys of a pass hit every bank exactly once per 16-byte load.
   float qn[16], qr[8];
   {
-    const uint16_t* qsrc = p.q_nope + bh * 128 + l8 * 16;
+    const uint16_t* qsrc = p.q_nope + bh * 128 + l8 * 8;
     load8(qsrc, p.scale_log2, qn);
-    load8(qsrc + 8, p.scale_log2, qn + 8);
+    load8(qsrc + 64, p.scale_log2, qn + 8);
     load8(p.q_pe + bh * 64 + l8 * 8, p.scale_log2, qr);
   }
 
@@ -188,9 +190,9 @@ __global__ void __launch_bounds__(DecCfg<G, T, NST, WPH>::kThreads, 1)
 #pragma unroll
       for (int ps = 0; ps < C::kPasses; ++ps) {
         const int t = wh * C::kTokPerWarp + ps * 4 + tk;
-        const uint8_t* krow = kn_s + t * 256 + l8 * 32;
+        const uint8_t* krow = kn_s + t * 256 + l8 * 16;
         const uint4 a0 = *reinterpret_cast<const uint4*>(krow);
-        const uint4 a1 = *reinterpret_cast<const uint4*>(krow + 16);
+        const uint4 a1 = *reinterpret_cast<const uint4*>(krow + 128);
         const uint4 c0 = *reinterpret_cast<const uint4*>(kpe_s + t * 128 + l8 * 16);
         float d = dot8(a0, qn) + dot8(a1, qn + 8) + dot8(c0, qr);
         d += __shfl_xor_sync(0xffffffffu, d, 1);

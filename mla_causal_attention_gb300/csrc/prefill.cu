@@ -42,7 +42,7 @@ namespace {
 constexpr int kBM = 128;       // query rows per tile (TMEM lanes)
 constexpr int kBN = 128;       // keys per tile
 constexpr int kSub = 16384;    // one 128-row x 128-byte (64 bf16) swizzled sub-tile
-constexpr int kSlots = 8;      // K/V ring depth in sub-tiles
+constexpr int kSlots = 8;      // K/V ring depth in sub-tiles (a power of two)
 constexpr int kSubPerKv = 5;   // kn0, kn1, kpe, v0, v1
 constexpr int kThreads = 384;
 constexpr int kOffQ = 0;                       // 2 tiles x {nope0, nope1, pe}
@@ -218,27 +218,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Every load this thread issued must land before shared memory is released.
       drain_wait(&bars->q_full, 0);
       for (int v = max(0, u - kSlots); v < u; ++v) drain_wait(&bars->full[v % kSlots], (v / kSlots) & 1);
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1) {
       // ================= MMA issuer =================
+      // The whole warp runs this loop (waits, descriptor arithmetic: warp-uniform values);
+      // one elected lane issues each batch of MMAs and commits.  Each MMA keeps the tensor
+      // core busy for only 32-64 cycles, so issue must be cheap: descriptors are built once
+      // (their high word is constant) and per MMA only the start-address field moves.
       constexpr uint32_t kIdescQK = tc::idesc_bf16_f32(128, 128, false);
       constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(128, 64, true);
-      bool ok = mbar_wait(&bars->q_full, 0, p.status, abort_flag);
+      constexpr uint32_t kSubLo = kSub >> 4;  // one sub-tile in descriptor address units
+      const uint64_t dhi = tc::smem_desc_sw128(0, 16, 1024);
+      const uint32_t q_lo = smem_u32(sQ) >> 4;
+      const uint32_t ring_lo = smem_u32(sRing) >> 4;
+      bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_full, 0, p.status, abort_flag));
       tc::fence_after_sync();
-      const uint32_t q_addr = smem_u32(sQ);
-      const uint32_t ring_addr = smem_u32(sRing);
       for (int j = 0; j <= n && ok; ++j) {
-        const int uk = j * kSubPerKv;         // first sub-tile of K(j)
-        const int uv = (j - 1) * kSubPerKv + 3;  // first sub-tile of V(j-1)
+        const uint32_t uk = (uint32_t)j * kSubPerKv;  // sub-tiles of K(j): uk .. uk+2
+        const uint32_t uv = uk - 2u;                   // sub-tiles of V(j-1): uv, uv+1
+        uint32_t klo[3], vlo[2];
+#pragma unroll
+        for (int s = 0; s < 3; ++s) klo[s] = ring_lo + ((uk + s) & (kSlots - 1)) * kSubLo;
+#pragma unroll
+        for (int s = 0; s < 2; ++s) vlo[s] = ring_lo + ((uv + s) & (kSlots - 1)) * kSubLo;
         if (j < n) {
           for (int s = 0; s < 3 && ok; ++s)
-            ok = mbar_wait(&bars->full[(uk + s) % kSlots], ((uk + s) / kSlots) & 1, p.status,
-                           abort_flag);
+            ok = mbar_wait(&bars->full[(uk + s) & (kSlots - 1)], ((uk + s) / kSlots) & 1,
+                           p.status, abort_flag);
         }
         if (j > 0) {
           for (int s = 0; s < 2 && ok; ++s)
-            ok = mbar_wait(&bars->full[(uv + s) % kSlots], ((uv + s) / kSlots) & 1, p.status,
-                           abort_flag);
+            ok = mbar_wait(&bars->full[(uv + s) & (kSlots - 1)], ((uv + s) / kSlots) & 1,
+                           p.status, abort_flag);
         }
+        ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc::fence_after_sync();
 #pragma unroll 1
@@ -247,49 +259,60 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t o_tmem = tbase + 256 + t * 128;
           if (j > 0 && j - 1 < nt[t]) {
             // O_t += P_t(j-1) V(j-1): P from TMEM (aliasing S_t), V MN-major from smem.
-            if (!mbar_wait(&bars->p_ready[t], (j - 1) & 1, p.status, abort_flag)) {
-              ok = false;
-              break;
-            }
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(&bars->p_ready[t], (j - 1) & 1, p.status, abort_flag));
+            if (!ok) break;
             tc::fence_after_sync();
+            const uint32_t acc0 = (j > 1) ? 1u : 0u;
+            if (tc::elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
+              for (int kk = 0; kk < 8; ++kk) {
 #pragma unroll
-              for (int hf = 0; hf < 2; ++hf) {
-                const uint32_t vaddr = ring_addr + ((uv + hf) % kSlots) * kSub + kk * 2048;
-                const uint64_t bdesc = tc::smem_desc_sw128(vaddr, 16, 1024);
-                tc::mma_ts(o_tmem + hf * 64, s_tmem + kk * 8, bdesc, kIdescPV,
-                           (j - 1 > 0 || kk > 0) ? 1u : 0u);
+                for (int hf = 0; hf < 2; ++hf) {
+                  const uint64_t bdesc = dhi | (uint64_t)(vlo[hf] + kk * (2048 >> 4));
+                  tc::mma_ts(o_tmem + hf * 64, s_tmem + kk * 8, bdesc, kIdescPV,
+                             kk > 0 ? 1u : acc0);
+                }
               }
+              if (j - 1 == nt[t] - 1) tc::commit(&bars->o_done[t]);
             }
-            if (j - 1 == nt[t] - 1) tc::commit(&bars->o_done[t]);
+            __syncwarp();
           }
           if (t == 1 && j > 0) {
             // V(j-1) is no longer needed once both value mixes have run.
-            tc::commit(&bars->empty[uv % kSlots]);
-            tc::commit(&bars->empty[(uv + 1) % kSlots]);
+            if (tc::elect_one()) {
+              tc::commit(&bars->empty[uv & (kSlots - 1)]);
+              tc::commit(&bars->empty[(uv + 1) & (kSlots - 1)]);
+            }
+            __syncwarp();
           }
           if (j < nt[t]) {
             // S_t = Q_t K(j)^T over 192 columns: 4 k-steps per 64-column sub-tile.
-            const uint32_t qa = q_addr + t * 3 * kSub;
+            const uint32_t qlo = q_lo + t * 3 * kSubLo;
+            if (tc::elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < 12; ++kk) {
-              const int sub = kk >> 2;
-              const uint32_t koff = (kk & 3) * 32;
-              const uint64_t adesc = tc::smem_desc_sw128(qa + sub * kSub + koff, 16, 1024);
-              const uint32_t kaddr = ring_addr + ((uk + sub) % kSlots) * kSub + koff;
-              const uint64_t bdesc = tc::smem_desc_sw128(kaddr, 16, 1024);
-              tc::mma_ss(s_tmem, adesc, bdesc, kIdescQK, kk > 0 ? 1u : 0u);
+              for (int kk = 0; kk < 12; ++kk) {
+                const uint32_t koff = (kk & 3) * (32 >> 4);
+                const uint64_t adesc = dhi | (uint64_t)(qlo + (kk >> 2) * kSubLo + koff);
+                const uint64_t bdesc = dhi | (uint64_t)(klo[kk >> 2] + koff);
+                tc::mma_ss(s_tmem, adesc, bdesc, kIdescQK, kk > 0 ? 1u : 0u);
+              }
+              tc::commit(&bars->s_full[t]);
             }
-            tc::commit(&bars->s_full[t]);
+            __syncwarp();
           }
         }
         if (j < n && ok) {
-          for (int s = 0; s < 3; ++s) tc::commit(&bars->empty[(uk + s) % kSlots]);
+          if (tc::elect_one()) {
+#pragma unroll
+            for (int s = 0; s < 3; ++s) tc::commit(&bars->empty[(uk + s) & (kSlots - 1)]);
+          }
+          __syncwarp();
         }
       }
       // No MMA may still be running when TMEM is released.
-      tc::commit(&bars->mma_done);
+      if (tc::elect_one()) tc::commit(&bars->mma_done);
+      __syncwarp();
       drain_wait(&bars->mma_done, 0);
     }
     __syncwarp();
@@ -328,11 +351,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 32; ++e)
             if (jt + c * 32 + e >= limit) r[c][e] = __float_as_uint(-INFINITY);
       }
-      float mx = -INFINITY;
+      // Row max over 8 independent chains (a single 128-long chain is latency-bound).
+      float mxp[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mxp[k] = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(r[c][e]));
+        for (int e = 0; e < 32; ++e) mxp[e & 7] = fmaxf(mxp[e & 7], __uint_as_float(r[c][e]));
+      const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
+                             fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
       const float m_tile = mx * sl2;
       if (j == 0) {
         m = m_tile;
@@ -357,7 +385,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const float neg_m = -m;
-      float sum0 = 0.f, sum1 = 0.f;
+      float sp[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) sp[k] = 0.f;
       uint32_t pk[2][32];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -365,12 +395,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 32; e += 2) {
           const float x0 = ex2_approx(fmaf(__uint_as_float(r[c][e]), sl2, neg_m));
           const float x1 = ex2_approx(fmaf(__uint_as_float(r[c][e + 1]), sl2, neg_m));
-          sum0 += x0;
-          sum1 += x1;
+          sp[(e >> 1) & 3] += x0;
+          sp[4 + ((e >> 1) & 3)] += x1;
           pk[c >> 1][(c & 1) * 16 + (e >> 1)] = pack_bf16x2(x0, x1);
         }
       }
-      l += sum0 + sum1;
+      l += ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
       tc::tmem_st32(s_tmem, pk[0]);
       tc::tmem_st32(s_tmem + 32, pk[1]);
       tc::tmem_wait_st();
