@@ -129,6 +129,62 @@ def _check(t, name, dtype, shape, device):
         raise ValueError(f"{name} must be contiguous")
 
 
+class PreparedCall:
+    """mla_attn_fwd with its tensors, workspace, stream and options fixed.
+
+    Construction validates everything once; each call re-enqueues the attention core with
+    one ctypes call (no per-call Python checks), which matters when the kernels themselves
+    take only microseconds.  The tensors are kept alive by this object.
+    """
+
+    def __init__(self, q_nope, q_pe, k_nope, k_pe_shared, v, kv_len, past_len: int,
+                 softmax_scale: float, out=None, workspace: "Workspace | None" = None,
+                 stream=None, path: int = PATH_AUTO, decode_chunk: int = 0):
+        lib = library()
+        dev = q_nope.device
+        if dev.type != "cuda":
+            raise ValueError("inputs must be CUDA tensors")
+        B, H, Tq = q_nope.shape[:3]
+        Tk = k_nope.shape[2]
+        bf = torch.bfloat16
+        _check(q_nope, "q_nope", bf, (B, H, Tq, 128), dev)
+        _check(q_pe, "q_pe", bf, (B, H, Tq, 64), dev)
+        _check(k_nope, "k_nope", bf, (B, H, Tk, 128), dev)
+        _check(k_pe_shared, "k_pe_shared", bf, (B, Tk, 64), dev)
+        _check(v, "v", bf, (B, H, Tk, 128), dev)
+        if kv_len is not None:
+            _check(kv_len, "kv_len", torch.int32, (B,), dev)
+        if out is None:
+            out = torch.empty((B, H, Tq, 128), dtype=bf, device=dev)
+        _check(out, "out", bf, (B, H, Tq, 128), dev)
+        ws_bytes = lib.mla_attn_workspace_bytes(B, H, Tq, Tk)
+        if decode_chunk:
+            splits = -(-Tk // decode_chunk)
+            ws_bytes = max(ws_bytes, 256 + (-(-B * H * splits * 8 // 256)) * 256
+                           + B * H * splits * 512)
+        ws = (workspace or _default_workspace(dev)).get(ws_bytes)
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        self.out = out
+        self.device = dev
+        self._keep = (q_nope, q_pe, k_nope, k_pe_shared, v, kv_len, out, ws, s)
+        self._opts = _Options(int(path), int(decode_chunk))
+        self._fn = lib.mla_attn_fwd_ex
+        self._args = (_ptr(q_nope), _ptr(q_pe), _ptr(k_nope), _ptr(k_pe_shared), _ptr(v),
+                      _ptr(kv_len), B, H, Tq, Tk, int(past_len), float(softmax_scale),
+                      _ptr(out), _ptr(ws), ws.numel(), ctypes.c_void_p(s.cuda_stream),
+                      ctypes.byref(self._opts))
+
+    def __call__(self):
+        if torch.cuda.current_device() != self.device.index:
+            with torch.cuda.device(self.device):
+                rc = self._fn(*self._args)
+        else:
+            rc = self._fn(*self._args)
+        if rc != 0:
+            raise MlaAttnError(rc, "mla_attn_fwd: ")
+        return self.out
+
+
 def mla_attn_fwd(q_nope, q_pe, k_nope, k_pe_shared, v, kv_len, past_len: int,
                  softmax_scale: float, out=None, workspace: Workspace | None = None,
                  stream=None, path: int = PATH_AUTO, decode_chunk: int = 0):
@@ -138,40 +194,8 @@ def mla_attn_fwd(q_nope, q_pe, k_nope, k_pe_shared, v, kv_len, past_len: int,
     v [B,H,Tk,128] (bf16, contiguous, CUDA); kv_len [B] int32 on the same device or None.
     Enqueued on ``stream`` (default: torch's current stream); returns ``out``.
     """
-    lib = library()
-    dev = q_nope.device
-    if dev.type != "cuda":
-        raise ValueError("inputs must be CUDA tensors")
-    B, H, Tq = q_nope.shape[:3]
-    Tk = k_nope.shape[2]
-    bf = torch.bfloat16
-    _check(q_nope, "q_nope", bf, (B, H, Tq, 128), dev)
-    _check(q_pe, "q_pe", bf, (B, H, Tq, 64), dev)
-    _check(k_nope, "k_nope", bf, (B, H, Tk, 128), dev)
-    _check(k_pe_shared, "k_pe_shared", bf, (B, Tk, 64), dev)
-    _check(v, "v", bf, (B, H, Tk, 128), dev)
-    if kv_len is not None:
-        _check(kv_len, "kv_len", torch.int32, (B,), dev)
-    if out is None:
-        out = torch.empty((B, H, Tq, 128), dtype=bf, device=dev)
-    _check(out, "out", bf, (B, H, Tq, 128), dev)
-    ws_bytes = lib.mla_attn_workspace_bytes(B, H, Tq, Tk)
-    if decode_chunk:
-        splits = -(-Tk // decode_chunk)
-        ws_bytes = max(ws_bytes, 256 + (-(-B * H * splits * 8 // 256)) * 256
-                       + B * H * splits * 512)
-    ws = (workspace or _default_workspace(dev)).get(ws_bytes)
-    s = stream if stream is not None else torch.cuda.current_stream(dev)
-    handle = ctypes.c_void_p(s.cuda_stream)
-    opts = _Options(int(path), int(decode_chunk))
-    with torch.cuda.device(dev):
-        rc = lib.mla_attn_fwd_ex(_ptr(q_nope), _ptr(q_pe), _ptr(k_nope), _ptr(k_pe_shared),
-                                 _ptr(v), _ptr(kv_len), B, H, Tq, Tk, int(past_len),
-                                 float(softmax_scale), _ptr(out), _ptr(ws), ws.numel(),
-                                 handle, ctypes.byref(opts))
-    if rc != 0:
-        raise MlaAttnError(rc, "mla_attn_fwd: ")
-    return out
+    return PreparedCall(q_nope, q_pe, k_nope, k_pe_shared, v, kv_len, past_len,
+                        softmax_scale, out, workspace, stream, path, decode_chunk)()
 
 
 def mla_attn_get_status(workspace: Workspace | None = None, device=None, stream=None) -> int:

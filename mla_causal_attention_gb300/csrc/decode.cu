@@ -101,6 +101,9 @@ __global__ void __launch_bounds__(DecCfg<G, T, NST, WPH>::kThreads, 1)
     if (threadIdx.x == 0 && hg == 0 && split == 0) set_status(p.status, MLA_ERR_KVLEN);
     kvl = min(max(kvl, 1), p.Tk);
   }
+  // Let the combine grid (launched with programmatic stream serialisation) get scheduled
+  // now; it waits for this grid's completion itself before reading any partial.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int j0 = split * p.chunk;
   if (j0 >= kvl) return;  // uniform across the CTA: this split holds no visible key
   const int j1 = min(j0 + p.chunk, kvl);
@@ -280,6 +283,9 @@ __global__ void __launch_bounds__(DecCfg<G, T, NST, WPH>::kThreads, 1)
 
 // One warp per (b, h): merge the partials of the splits that hold visible keys.
 __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeArgs p) {
+  // Launched as a programmatic dependent of the split kernel: wait until that grid has
+  // completed and its partials are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int w = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (w >= p.B * p.H) return;
@@ -333,9 +339,20 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess || a.splits == 1) return e;
+  // The combine pass is a programmatic dependent launch: its launch latency overlaps
+  // the tail of the split kernel.
   const int warps = a.B * a.H;
-  decode_combine_kernel<<<(warps + 7) / 8, 256, 0, stream>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((warps + 7) / 8);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_combine_kernel, a);
 }
 
 }  // namespace mla

@@ -16,7 +16,7 @@
 //                 S_t  = Q_t K_j^T     12 x (M128 N128 K16), A and B from shared memory,
 //                                      the 192-wide contraction split 64 | 64 | 64 so the
 //                                      concatenated key is never materialised;
-//                 O_t += P_t V_j       8 x 2 x (M128 N64 K16), P from TMEM, V from smem.
+//                 O_t += P_t V_j       8 x (M128 N128 K16), P from TMEM, V from smem.
 //               Order per key tile: PV_0(j-1), QK_0(j), PV_1(j-1), QK_1(j), so one
 //               softmax warpgroup works while the tensor core runs the other tile.
 //   warps 4-7   softmax of query tile 0 (thread = row = TMEM lane);
@@ -64,9 +64,13 @@ struct PrefillParams {
   float scale_log2;
 };
 
+// K/V tiles are tracked as groups (one K tile = 3 sub-tiles, one V tile = 2), double-
+// buffered by key-tile parity: at most two tiles of each kind are in flight.
 struct Bars {
-  uint64_t full[kSlots];
-  uint64_t empty[kSlots];
+  uint64_t kfull[2];   // K(j) landed (3 TMA boxes, one transaction count)
+  uint64_t vfull[2];   // V(j) landed (2 boxes)
+  uint64_t kempty[2];  // K(j) slots released (MMA commit after both score MMAs)
+  uint64_t vempty[2];  // V(j) slots released (MMA commit after both value mixes)
   uint64_t q_full;
   uint64_t s_full[2];
   uint64_t p_ready[2];
@@ -150,9 +154,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kSlots; ++i) {
-      mbar_init(&bars->full[i], 1);
-      mbar_init(&bars->empty[i], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->kfull[i], 1);
+      mbar_init(&bars->vfull[i], 1);
+      mbar_init(&bars->kempty[i], 1);
+      mbar_init(&bars->vempty[i], 1);
     }
     mbar_init(&bars->q_full, 1);
     for (int t = 0; t < 2; ++t) {
@@ -192,32 +198,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(sQ + (t * 3 + 1) * kSub, &p.tm_qn, &bars->q_full, 64, rt, bh, pol_q);
         tma_load_3d(sQ + (t * 3 + 2) * kSub, &p.tm_qr, &bars->q_full, 0, rt, bh, pol_q);
       }
-      int u = 0;
+      // Sub-tile u goes to slot u % kSlots, whose previous occupant was sub-tile
+      // u - kSlots of key tile (u - kSlots) / 5; that tile's K or V group must have been
+      // released by the MMAs before the slot is overwritten.
+      auto slot_free = [&](uint32_t u) -> bool {
+        if (u < (uint32_t)kSlots) return true;
+        const uint32_t prev = u - kSlots;
+        const uint32_t st = prev / kSubPerKv;
+        uint64_t* bar = (prev % kSubPerKv) < 3 ? &bars->kempty[st & 1] : &bars->vempty[st & 1];
+        return mbar_wait(bar, (st >> 1) & 1, p.status, abort_flag);
+      };
+      uint32_t u = 0;
       bool ok = true;
-      for (int j = 0; j < n && ok; ++j) {
+      int k_posted = 0, v_posted = 0;  // groups whose transaction count has been posted
+      for (int j = 0; j < n && ok; ++j, u += kSubPerKv) {
         const int jt = j * kBN;
-        for (int s = 0; s < kSubPerKv; ++s, ++u) {
-          const int slot = u % kSlots;
-          if (u >= kSlots &&
-              !mbar_wait(&bars->empty[slot], ((u / kSlots) - 1) & 1, p.status, abort_flag)) {
-            ok = false;
-            break;
+        // K(j): no-rope columns 0-63, 64-127 and the shared rotary tile, one barrier.
+        uint64_t* kb = &bars->kfull[j & 1];
+        for (int s = 0; s < 3 && ok; ++s) {
+          ok = slot_free(u + s);
+          if (!ok) break;
+          if (s == 0) {
+            mbar_arrive_expect_tx(kb, 3 * kSub);
+            k_posted = j + 1;
           }
-          uint8_t* dst = sRing + slot * kSub;
-          uint64_t* fb = &bars->full[slot];
-          mbar_arrive_expect_tx(fb, kSub);
-          switch (s) {
-            case 0: tma_load_3d_nohint(dst, &p.tm_kn, fb, 0, jt, bh); break;
-            case 1: tma_load_3d_nohint(dst, &p.tm_kn, fb, 64, jt, bh); break;
-            case 2: tma_load_3d_nohint(dst, &p.tm_kr, fb, 0, jt, b); break;
-            case 3: tma_load_3d_nohint(dst, &p.tm_v, fb, 0, jt, bh); break;
-            default: tma_load_3d_nohint(dst, &p.tm_v, fb, 64, jt, bh); break;
-          }
+          uint8_t* dst = sRing + ((u + s) & (kSlots - 1)) * kSub;
+          if (s < 2)
+            tma_load_3d_nohint(dst, &p.tm_kn, kb, 64 * s, jt, bh);
+          else
+            tma_load_3d_nohint(dst, &p.tm_kr, kb, 0, jt, b);
         }
+        if (!ok) break;
+        // V(j): columns 0-63 go to the lower-addressed of its two slots, so one MMA with a
+        // positive leading-byte offset covers all 128 value columns.
+        uint64_t* vb = &bars->vfull[j & 1];
+        const uint32_t sa = (u + 3) & (kSlots - 1), sb = (u + 4) & (kSlots - 1);
+        ok = slot_free(u + 3) && slot_free(u + 4);
+        if (!ok) break;
+        mbar_arrive_expect_tx(vb, 2 * kSub);
+        v_posted = j + 1;
+        tma_load_3d_nohint(sRing + min(sa, sb) * kSub, &p.tm_v, vb, 0, jt, bh);
+        tma_load_3d_nohint(sRing + max(sa, sb) * kSub, &p.tm_v, vb, 64, jt, bh);
       }
       // Every load this thread issued must land before shared memory is released.
       drain_wait(&bars->q_full, 0);
-      for (int v = max(0, u - kSlots); v < u; ++v) drain_wait(&bars->full[v % kSlots], (v / kSlots) & 1);
+      for (int j = max(0, k_posted - 2); j < k_posted; ++j)
+        drain_wait(&bars->kfull[j & 1], (j >> 1) & 1);
+      for (int j = max(0, v_posted - 2); j < v_posted; ++j)
+        drain_wait(&bars->vfull[j & 1], (j >> 1) & 1);
     } else if (warp == 1) {
       // ================= MMA issuer =================
       // The whole warp runs this loop (waits, descriptor arithmetic: warp-uniform values);
@@ -225,9 +253,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // core busy for only 32-64 cycles, so issue must be cheap: descriptors are built once
       // (their high word is constant) and per MMA only the start-address field moves.
       constexpr uint32_t kIdescQK = tc::idesc_bf16_f32(128, 128, false);
-      constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(128, 64, true);
+      constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(128, 128, true);
       constexpr uint32_t kSubLo = kSub >> 4;  // one sub-tile in descriptor address units
-      const uint64_t dhi = tc::smem_desc_sw128(0, 16, 1024);
+      // K-major operands: leading offset unused, 8-row groups 1024 B apart.  V (MN-major):
+      // the two 64-column halves are one slot apart, or kSlots - 1 slots when the pair
+      // wraps around the ring; 8-key groups 1024 B apart.
+      const uint64_t dhi_k = tc::smem_desc_sw128(0, 16, 1024);
+      const uint64_t dhi_v_near = tc::smem_desc_sw128(0, kSub, 1024);
+      const uint64_t dhi_v_far = tc::smem_desc_sw128(0, (kSlots - 1) * kSub, 1024);
       const uint32_t q_lo = smem_u32(sQ) >> 4;
       const uint32_t ring_lo = smem_u32(sRing) >> 4;
       bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_full, 0, p.status, abort_flag));
@@ -235,24 +268,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j <= n && ok; ++j) {
         const uint32_t uk = (uint32_t)j * kSubPerKv;  // sub-tiles of K(j): uk .. uk+2
         const uint32_t uv = uk - 2u;                   // sub-tiles of V(j-1): uv, uv+1
-        uint32_t klo[3], vlo[2];
+        uint32_t klo[3];
 #pragma unroll
         for (int s = 0; s < 3; ++s) klo[s] = ring_lo + ((uk + s) & (kSlots - 1)) * kSubLo;
-#pragma unroll
-        for (int s = 0; s < 2; ++s) vlo[s] = ring_lo + ((uv + s) & (kSlots - 1)) * kSubLo;
-        if (j < n) {
-          for (int s = 0; s < 3 && ok; ++s)
-            ok = mbar_wait(&bars->full[(uk + s) & (kSlots - 1)], ((uk + s) / kSlots) & 1,
-                           p.status, abort_flag);
-        }
-        if (j > 0) {
-          for (int s = 0; s < 2 && ok; ++s)
-            ok = mbar_wait(&bars->full[(uv + s) & (kSlots - 1)], ((uv + s) / kSlots) & 1,
-                           p.status, abort_flag);
-        }
+        const uint32_t va = uv & (kSlots - 1), vb2 = (uv + 1) & (kSlots - 1);
+        const uint32_t vlo = ring_lo + min(va, vb2) * kSubLo;
+        const uint64_t dhi_v = vb2 > va ? dhi_v_near : dhi_v_far;
+        // V(j-1) first: the value mix of tile 0 can start while K(j) is still landing.
+        if (j > 0) ok = mbar_wait(&bars->vfull[(j - 1) & 1], ((j - 1) >> 1) & 1, p.status, abort_flag);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc::fence_after_sync();
+        bool k_landed = false;
 #pragma unroll 1
         for (int t = 0; t < 2; ++t) {
           const uint32_t s_tmem = tbase + t * 128;
@@ -267,12 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (tc::elect_one()) {
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk) {
-#pragma unroll
-                for (int hf = 0; hf < 2; ++hf) {
-                  const uint64_t bdesc = dhi | (uint64_t)(vlo[hf] + kk * (2048 >> 4));
-                  tc::mma_ts(o_tmem + hf * 64, s_tmem + kk * 8, bdesc, kIdescPV,
-                             kk > 0 ? 1u : acc0);
-                }
+                const uint64_t bdesc = dhi_v | (uint64_t)(vlo + kk * (2048 >> 4));
+                tc::mma_ts(o_tmem, s_tmem + kk * 8, bdesc, kIdescPV, kk > 0 ? 1u : acc0);
               }
               if (j - 1 == nt[t] - 1) tc::commit(&bars->o_done[t]);
             }
@@ -280,21 +303,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (t == 1 && j > 0) {
             // V(j-1) is no longer needed once both value mixes have run.
-            if (tc::elect_one()) {
-              tc::commit(&bars->empty[uv & (kSlots - 1)]);
-              tc::commit(&bars->empty[(uv + 1) & (kSlots - 1)]);
-            }
+            if (tc::elect_one()) tc::commit(&bars->vempty[(j - 1) & 1]);
             __syncwarp();
           }
           if (j < nt[t]) {
+            if (!k_landed) {
+              ok = __all_sync(0xffffffffu,
+                              mbar_wait(&bars->kfull[j & 1], (j >> 1) & 1, p.status, abort_flag));
+              if (!ok) break;
+              tc::fence_after_sync();
+              k_landed = true;
+            }
             // S_t = Q_t K(j)^T over 192 columns: 4 k-steps per 64-column sub-tile.
             const uint32_t qlo = q_lo + t * 3 * kSubLo;
             if (tc::elect_one()) {
 #pragma unroll
               for (int kk = 0; kk < 12; ++kk) {
                 const uint32_t koff = (kk & 3) * (32 >> 4);
-                const uint64_t adesc = dhi | (uint64_t)(qlo + (kk >> 2) * kSubLo + koff);
-                const uint64_t bdesc = dhi | (uint64_t)(klo[kk >> 2] + koff);
+                const uint64_t adesc = dhi_k | (uint64_t)(qlo + (kk >> 2) * kSubLo + koff);
+                const uint64_t bdesc = dhi_k | (uint64_t)(klo[kk >> 2] + koff);
                 tc::mma_ss(s_tmem, adesc, bdesc, kIdescQK, kk > 0 ? 1u : 0u);
               }
               tc::commit(&bars->s_full[t]);
@@ -303,10 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (j < n && ok) {
-          if (tc::elect_one()) {
-#pragma unroll
-            for (int s = 0; s < 3; ++s) tc::commit(&bars->empty[(uk + s) & (kSlots - 1)]);
-          }
+          if (tc::elect_one()) tc::commit(&bars->kempty[j & 1]);
           __syncwarp();
         }
       }
@@ -484,19 +508,70 @@ bool encode_3d(EncodeTiledFn fn, CUtensorMap* m, const void* base, uint64_t inne
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Host-side cache of encoded tensor maps, keyed by the five input pointers and the sizes:
+// a serving loop calls the same buffers over and over, and encoding costs microseconds.
+struct MapKey {
+  const void* ptr[5];
+  int B, H, Tq, Tk;
+  bool operator==(const MapKey& o) const {
+    for (int i = 0; i < 5; ++i)
+      if (ptr[i] != o.ptr[i]) return false;
+    return B == o.B && H == o.H && Tq == o.Tq && Tk == o.Tk;
+  }
+};
+struct MapEntry {
+  MapKey key;
+  CUtensorMap maps[5];
+  bool valid;
+};
+constexpr int kMapCacheSize = 16;
+std::mutex g_map_mu;
+MapEntry g_map_cache[kMapCacheSize];
+int g_map_next = 0;
+
+bool tensor_maps(const PrefillArgs& a, PrefillParams* p) {
+  const MapKey key = {{a.q_nope, a.q_pe, a.k_nope, a.k_pe, a.v}, a.B, a.H, a.Tq, a.Tk};
+  {
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    for (const MapEntry& e : g_map_cache) {
+      if (e.valid && e.key == key) {
+        p->tm_qn = e.maps[0];
+        p->tm_qr = e.maps[1];
+        p->tm_kn = e.maps[2];
+        p->tm_kr = e.maps[3];
+        p->tm_v = e.maps[4];
+        return true;
+      }
+    }
+  }
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  const uint64_t BH = (uint64_t)a.B * a.H;
+  if (!encode_3d(fn, &p->tm_qn, a.q_nope, 128, a.Tq, BH) ||
+      !encode_3d(fn, &p->tm_qr, a.q_pe, 64, a.Tq, BH) ||
+      !encode_3d(fn, &p->tm_kn, a.k_nope, 128, a.Tk, BH) ||
+      !encode_3d(fn, &p->tm_kr, a.k_pe, 64, a.Tk, a.B) ||
+      !encode_3d(fn, &p->tm_v, a.v, 128, a.Tk, BH))
+    return false;
+  std::lock_guard<std::mutex> lk(g_map_mu);
+  MapEntry& e = g_map_cache[g_map_next];
+  g_map_next = (g_map_next + 1) % kMapCacheSize;
+  e.key = key;
+  e.maps[0] = p->tm_qn;
+  e.maps[1] = p->tm_qr;
+  e.maps[2] = p->tm_kn;
+  e.maps[3] = p->tm_kr;
+  e.maps[4] = p->tm_v;
+  e.valid = true;
+  return true;
+}
+
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
-  EncodeTiledFn fn = get_encode_fn();
-  if (!fn) return cudaErrorNotSupported;
   PrefillParams p;
+  if (!tensor_maps(a, &p)) return cudaErrorInvalidValue;
   const uint64_t BH = (uint64_t)a.B * a.H;
-  if (!encode_3d(fn, &p.tm_qn, a.q_nope, 128, a.Tq, BH) ||
-      !encode_3d(fn, &p.tm_qr, a.q_pe, 64, a.Tq, BH) ||
-      !encode_3d(fn, &p.tm_kn, a.k_nope, 128, a.Tk, BH) ||
-      !encode_3d(fn, &p.tm_kr, a.k_pe, 64, a.Tk, a.B) ||
-      !encode_3d(fn, &p.tm_v, a.v, 128, a.Tk, BH))
-    return cudaErrorInvalidValue;
   p.kv_len = a.kv_len;
   p.out = a.out;
   p.status = a.status;
