@@ -73,7 +73,7 @@ struct Bars {
   uint64_t vempty[2];  // V(j) slots released (MMA commit after both value mixes)
   uint64_t q_full;
   uint64_t s_full[2];
-  uint64_t p_ready[2];
+  uint64_t p_ready[2];  // P_t written to TMEM (4 warp arrivals)
   uint64_t o_done[2];
   uint64_t mma_done;
   uint32_t tmem_base;
@@ -375,16 +375,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 32; ++e)
             if (jt + c * 32 + e >= limit) r[c][e] = __float_as_uint(-INFINITY);
       }
-      // Row max over 8 independent chains (a single 128-long chain is latency-bound).
+      // Row max: 8 independent chains of three-input maxima (64 instructions for 128
+      // scores; a single 128-long chain would be latency-bound).
       float mxp[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mxp[k] = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int e = 0; e < 32; ++e) mxp[e & 7] = fmaxf(mxp[e & 7], __uint_as_float(r[c][e]));
-      const float mx = fmaxf(fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3])),
-                             fmaxf(fmaxf(mxp[4], mxp[5]), fmaxf(mxp[6], mxp[7])));
+        for (int e = 0; e < 32; e += 2)
+          mxp[(e >> 1) & 7] = fmax3(mxp[(e >> 1) & 7], __uint_as_float(r[c][e]),
+                                    __uint_as_float(r[c][e + 1]));
+      const float mx = fmax3(fmax3(mxp[0], mxp[1], mxp[2]), fmax3(mxp[3], mxp[4], mxp[5]),
+                             fmaxf(mxp[6], mxp[7]));
       const float m_tile = mx * sl2;
       if (j == 0) {
         m = m_tile;
@@ -408,23 +411,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      const float neg_m = -m;
-      float sp[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) sp[k] = 0.f;
+      // p = 2^(s * scale * log2(e) - m): the scale-and-subtract and the row sum run on
+      // fp32 pairs (one instruction per two scores), the exponentials on the MUFU.
+      const uint64_t sl2_2 = f2_pack(sl2, sl2);
+      const uint64_t negm_2 = f2_pack(-m, -m);
+      uint64_t sp2[4] = {0ull, 0ull, 0ull, 0ull};
       uint32_t pk[2][32];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const float x0 = ex2_approx(fmaf(__uint_as_float(r[c][e]), sl2, neg_m));
-          const float x1 = ex2_approx(fmaf(__uint_as_float(r[c][e + 1]), sl2, neg_m));
-          sp[(e >> 1) & 3] += x0;
-          sp[4 + ((e >> 1) & 3)] += x1;
+          const uint64_t xv = ffma2(
+              f2_pack(__uint_as_float(r[c][e]), __uint_as_float(r[c][e + 1])), sl2_2, negm_2);
+          float x0, x1;
+          f2_unpack(xv, x0, x1);
+          x0 = ex2_approx(x0);
+          x1 = ex2_approx(x1);
+          sp2[(e >> 1) & 3] = fadd2(sp2[(e >> 1) & 3], f2_pack(x0, x1));
           pk[c >> 1][(c & 1) * 16 + (e >> 1)] = pack_bf16x2(x0, x1);
         }
       }
-      l += ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+      float sa, sb;
+      f2_unpack(fadd2(fadd2(sp2[0], sp2[1]), fadd2(sp2[2], sp2[3])), sa, sb);
+      l += sa + sb;
       tc::tmem_st32(s_tmem, pk[0]);
       tc::tmem_st32(s_tmem + 32, pk[1]);
       tc::tmem_wait_st();
