@@ -15,6 +15,7 @@
 // writes either the final bf16 row (single split) or a (max, sum, acc[128]) partial that
 // the combine kernel merges:  m = max m_s,  l = sum 2^(m_s - m) l_s,
 // out = sum 2^(m_s - m) acc_s / l.
+#include <atomic>
 #include <cmath>
 
 #include "kernels.h"
@@ -79,8 +80,8 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-template <int G, int T, int NST, int WPH>
-__global__ void __launch_bounds__(DecCfg<G, T, NST, WPH>::kThreads, 1)
+template <int G, int T, int NST, int WPH, int MINB>
+__global__ void __launch_bounds__(DecCfg<G, T, NST, WPH>::kThreads, MINB)
     decode_splitkv_kernel(const DecodeArgs p) {
   using C = DecCfg<G, T, NST, WPH>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -317,27 +318,34 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeArgs p)
   *reinterpret_cast<uint2*>(p.out + (size_t)w * 128 + lane * 4) = o;
 }
 
-using DecKernelCfg = DecCfg<kDecHeadsPerCta, kDecTokensPerStage, 3, 2>;
+template <int T, int MINB>
+cudaError_t launch_split(const DecodeArgs& a, cudaStream_t stream) {
+  constexpr int G = kDecHeadsPerCta, NST = 3, WPH = 2;
+  using C = DecCfg<G, T, NST, WPH>;
+  auto kern = decode_splitkv_kernel<G, T, NST, WPH, MINB>;
+  static std::atomic<uint64_t> attr_done{0};  // bit per device: smem attribute set
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(attr_done.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_done.fetch_or(bit, std::memory_order_release);
+  }
+  dim3 grid((a.H + G - 1) / G, a.splits, a.B);
+  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(a);
+  return cudaGetLastError();
+}
 
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
-  constexpr int G = kDecHeadsPerCta, T = kDecTokensPerStage, NST = 3, WPH = 2;
-  using C = DecCfg<G, T, NST, WPH>;
-  auto kern = decode_splitkv_kernel<G, T, NST, WPH>;
-  static int attr_device = -1;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (attr_device != dev) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)C::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_device = dev;
-  }
-  dim3 grid((a.H + G - 1) / G, a.splits, a.B);
-  kern<<<grid, C::kThreads, C::kSmemBytes, stream>>>(a);
-  e = cudaGetLastError();
+  // Large problems: 32-key stages, 1 CTA per SM (213 KB of stages in flight per SM).
+  // Small problems: 16-key stages, 2 CTAs per SM, so the grid fits in one wave.
+  cudaError_t e = a.small ? launch_split<kDecTokensPerStage / 2, 2>(a, stream)
+                          : launch_split<kDecTokensPerStage, 1>(a, stream);
   if (e != cudaSuccess || a.splits == 1) return e;
   // The combine pass is a programmatic dependent launch: its launch latency overlaps
   // the tail of the split kernel.

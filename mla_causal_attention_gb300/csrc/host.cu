@@ -5,6 +5,7 @@
 // the scores must have shape [B, H, Tq, Tk] with Tk the cached length plus the new
 // rows, and a mask must be present (here it is implied by past_len and kv_len, so it is
 // always present).  Failing checks return an error code; nothing is launched.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -54,20 +55,6 @@ mla_status check_shape(int B, int H, int Tq, int Tk, int past_len) {
   return MLA_OK;
 }
 
-// Keys per split for the decode path: the largest power-of-two multiple of 64 (at most
-// 1024) that still leaves two full waves of CTAs on the GPU at one CTA per SM.
-void plan_decode(int B, int H, int Tk, int sms, int* chunk, int* splits) {
-  const int64_t groups = (int64_t)B * ((H + kDecHeadsPerCta - 1) / kDecHeadsPerCta);
-  int c = kDecMinChunk;
-  while (c < 1024) {
-    const int64_t next = groups * ((Tk + 2 * c - 1) / (2 * c));
-    if (next < 2 * (int64_t)sms) break;
-    c *= 2;
-  }
-  *chunk = c;
-  *splits = (Tk + c - 1) / c;
-}
-
 // Partials: (max, sum) pairs, then the 128-float accumulators starting on a 256-byte
 // boundary (the kernels access them with 16-byte vector loads and stores).
 size_t decode_ml_bytes(int B, int H, int splits) {
@@ -82,6 +69,35 @@ size_t decode_workspace(int B, int H, int splits) {
 }
 
 }  // namespace
+
+// Keys per split for the decode path.  When there are at least as many (sequence, head
+// group) units as SMs, the large configuration (32-key stages, 1 CTA per SM) takes the
+// largest power-of-two multiple of 64 keys (at most 1024) that still leaves two full
+// waves.  Smaller problems use the small configuration (16-key stages, 2 CTAs per SM) and
+// split the keys so that the whole grid is about one wave of 2 CTAs per SM.
+DecodePlan plan_decode(int B, int H, int Tk, int sms, int forced_chunk) {
+  const int64_t groups = (int64_t)B * ((H + kDecHeadsPerCta - 1) / kDecHeadsPerCta);
+  DecodePlan pl;
+  pl.small = groups < (int64_t)sms ? 1 : 0;
+  if (forced_chunk > 0) {
+    pl.chunk = forced_chunk;
+  } else if (!pl.small) {
+    int c = kDecMinChunk;
+    while (c < 1024) {
+      const int64_t next = groups * ((Tk + 2 * c - 1) / (2 * c));
+      if (next < 2 * (int64_t)sms) break;
+      c *= 2;
+    }
+    pl.chunk = c;
+  } else {
+    const int64_t want = std::max<int64_t>(1, (2 * (int64_t)sms) / groups);
+    int64_t c = (Tk + want - 1) / want;
+    c = std::max<int64_t>(32, (c + 31) / 32 * 32);
+    pl.chunk = (int)std::min<int64_t>(c, kDecMaxChunk);
+  }
+  pl.splits = (Tk + pl.chunk - 1) / pl.chunk;
+  return pl;
+}
 
 int device_sm_count() {
   int sms = 0;
@@ -114,10 +130,9 @@ mla_status mla_attn_decode_plan(int B, int H, int Tk, int* chunk, int* splits) {
   if (B < 1 || H < 1 || Tk < 1) return MLA_ERR_SHAPE;
   int sms = 0;
   if (check_device(&sms) != MLA_OK || sms <= 0) sms = 152;  // GB300 SM count when no device
-  int c = 0, s = 0;
-  plan_decode(B, H, Tk, sms, &c, &s);
-  if (chunk) *chunk = c;
-  if (splits) *splits = s;
+  const DecodePlan pl = plan_decode(B, H, Tk, sms, 0);
+  if (chunk) *chunk = pl.chunk;
+  if (splits) *splits = pl.splits;
   return MLA_OK;
 }
 
@@ -157,15 +172,12 @@ mla_status mla_attn_fwd_ex(const uint16_t* q_nope, const uint16_t* q_pe,
   const float scale_log2 = softmax_scale * 1.4426950408889634f;
 
   if (path == MLA_PATH_DECODE) {
-    int chunk = 0, splits = 0;
-    plan_decode(B, H, Tk, sms, &chunk, &splits);
     const int forced = options ? options->decode_chunk : 0;
-    if (forced != 0) {
-      if (forced < kDecMinChunk || forced > kDecMaxChunk || forced % kDecMinChunk != 0)
-        return MLA_ERR_ARG;
-      chunk = forced;
-      splits = (Tk + chunk - 1) / chunk;
-    }
+    if (forced != 0 &&
+        (forced < kDecMinChunk || forced > kDecMaxChunk || forced % kDecMinChunk != 0))
+      return MLA_ERR_ARG;
+    const DecodePlan pl = plan_decode(B, H, Tk, sms, forced);
+    const int chunk = pl.chunk, splits = pl.splits;
     if (splits > 65535) return MLA_ERR_ARG;
     if (workspace_bytes < decode_workspace(B, H, splits)) return MLA_ERR_WORKSPACE;
     DecodeArgs a;
@@ -174,7 +186,7 @@ mla_status mla_attn_fwd_ex(const uint16_t* q_nope, const uint16_t* q_pe,
     uint8_t* part = static_cast<uint8_t*>(workspace) + kStatusBytes;
     a.part_ml = reinterpret_cast<float*>(part);
     a.part_acc = reinterpret_cast<float*>(part + decode_ml_bytes(B, H, splits));
-    a.B = B; a.H = H; a.Tk = Tk; a.chunk = chunk; a.splits = splits;
+    a.B = B; a.H = H; a.Tk = Tk; a.chunk = chunk; a.splits = splits; a.small = pl.small;
     a.scale_log2 = scale_log2;
     return launch_decode(a, stream) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
   }

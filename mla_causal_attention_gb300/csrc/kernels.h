@@ -21,8 +21,9 @@ struct DecodeArgs {
   float* part_acc;
   int* status;
   int B, H, Tk;
-  int chunk;   // keys per split (multiple of the stage size)
+  int chunk;   // keys per split
   int splits;  // ceil(Tk / chunk)
+  int small;   // 1: 16-key stages, 2 CTAs per SM (problems smaller than one wave)
   float scale_log2;  // softmax_scale * log2(e)
 };
 
@@ -33,6 +34,14 @@ constexpr int kDecMinChunk = 64;
 constexpr int kDecMaxChunk = 65536;
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+// The decode scheduler's choice for given sizes on a GPU with `sms` SMs.
+struct DecodePlan {
+  int chunk;
+  int splits;
+  int small;
+};
+DecodePlan plan_decode(int B, int H, int Tk, int sms, int forced_chunk);
 
 // Prefill (Tq >= 1): fused tensor-core kernel.
 struct PrefillArgs {

@@ -70,16 +70,15 @@ extern "C" mla_status mla_attn_decode_noalloc(const uint16_t* q_nope, const uint
   if (device_sm_count() <= 0) return MLA_ERR_DEVICE;
 
   // Same split plan as mla_attn_fwd's decode path, so the two give identical results.
-  int chunk = 0, splits = 0;
-  mla_status st = mla_attn_decode_plan(B, H, Tk, &chunk, &splits);
-  if (st != MLA_OK) return st;
+  const DecodePlan pl = plan_decode(B, H, Tk, device_sm_count(), 0);
+  const int chunk = pl.chunk, splits = pl.splits;
   const size_t rows = (size_t)B * H * splits;
   const size_t ml_bytes = (rows * 2 * sizeof(float) + 255) & ~(size_t)255;
   const size_t need = splits > 1 ? ml_bytes + rows * 128 * sizeof(float) : 0;
   if (need > kNoAllocScratchBytes) return MLA_ERR_WORKSPACE;
 
   uint8_t* scratch = nullptr;
-  st = scratch_for_current_device(&scratch);
+  const mla_status st = scratch_for_current_device(&scratch);
   if (st != MLA_OK) return st;
 
   DecodeArgs a;
@@ -98,6 +97,7 @@ extern "C" mla_status mla_attn_decode_noalloc(const uint16_t* q_nope, const uint
   a.Tk = Tk;
   a.chunk = chunk;
   a.splits = splits;
+  a.small = pl.small;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   return launch_decode(a, static_cast<cudaStream_t>(cuda_stream)) == cudaSuccess ? MLA_OK
                                                                                  : MLA_ERR_CUDA;

@@ -66,9 +66,13 @@ def test_workspace_keeps_accumulators_16_byte_aligned(lib):
 def test_decode_plan_is_sane(lib):
     for B, H, Tk in [(1, 64, 1001), (64, 64, 8192), (3, 5, 17), (1, 1, 1)]:
         c, s = binding.decode_plan(B, H, Tk)
-        assert 64 <= c <= 1024 and c % 64 == 0
+        assert 32 <= c <= 1024 and c % 32 == 0
         assert (s - 1) * c < Tk <= s * c
-    assert binding.decode_plan(1, 64, 1001)[0] == 64
+    import torch
+    if not torch.cuda.is_available():  # the plan assumes GB300's 152 SMs without a device
+        # one sequence of 64 heads is smaller than a wave: about 2 CTAs per SM
+        assert binding.decode_plan(1, 64, 1001) == (64, 16)
+        assert binding.decode_plan(64, 64, 8192) == (1024, 8)
 
 
 def _call(lib, ptrs, B=1, H=1, Tq=2, Tk=2, past=0, scale=0.1, ws=256, opts=None):
