@@ -360,21 +360,18 @@ def cpu_baseline(wl, host, m, target_s):
     rng = np.random.default_rng(1234)
     args = (host["q_nope"], host["q_pe"], host["k_nope"], host["k_pe_shared"], host["v"],
             host["kv_len"], wl.past_len, wl.softmax_scale)
+    total_rows = wl.B * wl.H * wl.Tq
     n = max(threads, 8)
-    rows, work = _sample_rows(wl, host["kv_len"].numpy(), n, rng)
-    t0 = time.perf_counter()
-    oracle_rows(*args, rows=rows, threads=threads)
-    dt = time.perf_counter() - t0
-    rate = work / max(dt, 1e-6)
-    # grow the sample to about target_s seconds of oracle work
-    want = int(n * min(max(target_s / max(dt, 1e-6), 1.0), 1e6))
-    want = min(want, wl.B * wl.H * wl.Tq)
-    if want > n:
-        rows, work = _sample_rows(wl, host["kv_len"].numpy(), want, rng)
+    # Grow the sample until one timed run lasts about target_s seconds (or covers every row).
+    while True:
+        rows, work = _sample_rows(wl, host["kv_len"].numpy(), min(n, total_rows), rng)
         t0 = time.perf_counter()
         oracle_rows(*args, rows=rows, threads=threads)
         dt = time.perf_counter() - t0
-        rate = work / dt
+        if dt >= 0.8 * target_s or n >= total_rows:
+            break
+        n = int(n * min(max(1.5, target_s / max(dt, 1e-3)), 64.0))
+    rate = work / dt
     return {"value": rate * m["scale"], "unit": m["unit"], "cores": threads, "kind": "oracle",
             "sample": f"{len(rows)} random output rows of {wl.name} (full key range each), "
                       f"{dt:.1f} s on {threads} threads", "seconds": dt}
