@@ -128,6 +128,35 @@ MLA_API mla_status mla_attn_fwd_ex(const uint16_t* q_nope, const uint16_t* q_pe,
                            const mla_attn_options* options);
 
 /*
+ * Cache append + attention.  The cache update of the attention excerpt on "Kimi K2 ·
+ * Similarities" (past_key_value.update: the new key/value rows follow the cached prefix)
+ * fused with the core described at the top of this file:
+ *
+ *   k_nope_cache[b,h,past_len+t,:] = k_nope_new[b,h,t,:]    (t < Tq)
+ *   k_pe_cache  [b,  past_len+t,:] = k_pe_new  [b,  t,:]
+ *   v_cache     [b,h,past_len+t,:] = v_new     [b,h,t,:]
+ *   out = attention over rows [0, Tk) of the caches, Tk = past_len + Tq
+ *
+ * Caches: k_nope_cache / v_cache [B, H, T_cap, 128], k_pe_cache [B, T_cap, 64], device,
+ * T_cap >= past_len + Tq rows per (b, h) (per b for k_pe); rows outside [past_len, Tk) are
+ * not written.  New rows: k_nope_new / v_new [B, H, Tq, 128], k_pe_new [B, Tq, 64].  The
+ * other arguments are those of mla_attn_fwd (kv_len, when given, still hides keys >=
+ * kv_len[b]; the new rows are written at past_len regardless).  With Tq == 1 the append
+ * is fused into the decode kernel (the stage holding the new row reads it from the new
+ * buffers; one CTA per head group writes it to the cache); with Tq > 1 a copy kernel
+ * appends the rows before the attention kernel runs.  Errors as for mla_attn_fwd;
+ * MLA_ERR_SHAPE also when past_len + Tq > T_cap.
+ */
+MLA_API mla_status mla_attn_append_fwd(const uint16_t* q_nope, const uint16_t* q_pe,
+                                       const uint16_t* k_nope_new, const uint16_t* k_pe_new,
+                                       const uint16_t* v_new, uint16_t* k_nope_cache,
+                                       uint16_t* k_pe_cache, uint16_t* v_cache,
+                                       const int32_t* kv_len, int B, int H, int Tq, int T_cap,
+                                       int past_len, float softmax_scale, uint16_t* out,
+                                       void* workspace, size_t workspace_bytes,
+                                       void* cuda_stream);
+
+/*
  * Synchronises cuda_stream, reads the device status word in the workspace, clears it,
  * and returns it (MLA_OK if no kernel recorded a problem since the last read).
  */

@@ -8,7 +8,8 @@ the input generator and workload tables can be used without a GPU.
 from .workloads import WORKLOADS, Workload  # noqa: F401
 
 _BINDING_NAMES = ("MlaAttnError", "mla_attn_fwd", "mla_attn_workspace_bytes",
-                  "mla_attn_get_status", "library", "Workspace", "MlaStatus", "PreparedCall")
+                  "mla_attn_get_status", "library", "Workspace", "MlaStatus", "PreparedCall",
+                  "mla_attn_append_fwd")
 
 
 def __getattr__(name):

@@ -48,7 +48,8 @@ class _Options(ctypes.Structure):
 
 
 EXPORTED = ("mla_attn_workspace_bytes", "mla_attn_fwd", "mla_attn_fwd_ex",
-            "mla_attn_get_status", "mla_status_string", "mla_attn_decode_plan")
+            "mla_attn_get_status", "mla_status_string", "mla_attn_decode_plan",
+            "mla_attn_append_fwd")
 
 
 def library():
@@ -76,6 +77,9 @@ def library():
         lib.mla_status_string.argtypes = [i]
         lib.mla_attn_decode_plan.restype = i
         lib.mla_attn_decode_plan.argtypes = [i, i, i, ctypes.POINTER(i), ctypes.POINTER(i)]
+        lib.mla_attn_append_fwd.restype = i
+        lib.mla_attn_append_fwd.argtypes = [p, p, p, p, p, p, p, p, p, i, i, i, i, i, f, p, p,
+                                            sz, p]
         _lib = lib
         return lib
 
@@ -196,6 +200,46 @@ def mla_attn_fwd(q_nope, q_pe, k_nope, k_pe_shared, v, kv_len, past_len: int,
     """
     return PreparedCall(q_nope, q_pe, k_nope, k_pe_shared, v, kv_len, past_len,
                         softmax_scale, out, workspace, stream, path, decode_chunk)()
+
+
+def mla_attn_append_fwd(q_nope, q_pe, k_nope_new, k_pe_new, v_new, k_nope_cache,
+                        k_pe_cache, v_cache, kv_len, past_len: int, softmax_scale: float,
+                        out=None, workspace: "Workspace | None" = None, stream=None):
+    """Append the new key/value rows at [past_len, past_len + Tq) of the caches, then
+    attend over rows [0, past_len + Tq).  Caches: k_nope_cache / v_cache [B,H,T_cap,128],
+    k_pe_cache [B,T_cap,64]; new rows [B,H,Tq,128] / [B,Tq,64] / [B,H,Tq,128]."""
+    lib = library()
+    dev = q_nope.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    B, H, Tq = q_nope.shape[:3]
+    T_cap = k_nope_cache.shape[2]
+    bf = torch.bfloat16
+    _check(q_nope, "q_nope", bf, (B, H, Tq, 128), dev)
+    _check(q_pe, "q_pe", bf, (B, H, Tq, 64), dev)
+    _check(k_nope_new, "k_nope_new", bf, (B, H, Tq, 128), dev)
+    _check(k_pe_new, "k_pe_new", bf, (B, Tq, 64), dev)
+    _check(v_new, "v_new", bf, (B, H, Tq, 128), dev)
+    _check(k_nope_cache, "k_nope_cache", bf, (B, H, T_cap, 128), dev)
+    _check(k_pe_cache, "k_pe_cache", bf, (B, T_cap, 64), dev)
+    _check(v_cache, "v_cache", bf, (B, H, T_cap, 128), dev)
+    if kv_len is not None:
+        _check(kv_len, "kv_len", torch.int32, (B,), dev)
+    if out is None:
+        out = torch.empty((B, H, Tq, 128), dtype=bf, device=dev)
+    _check(out, "out", bf, (B, H, Tq, 128), dev)
+    ws = (workspace or _default_workspace(dev)).get(
+        lib.mla_attn_workspace_bytes(B, H, Tq, past_len + Tq))
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        rc = lib.mla_attn_append_fwd(_ptr(q_nope), _ptr(q_pe), _ptr(k_nope_new),
+                                     _ptr(k_pe_new), _ptr(v_new), _ptr(k_nope_cache),
+                                     _ptr(k_pe_cache), _ptr(v_cache), _ptr(kv_len), B, H, Tq,
+                                     T_cap, int(past_len), float(softmax_scale), _ptr(out),
+                                     _ptr(ws), ws.numel(), ctypes.c_void_p(s.cuda_stream))
+    if rc != 0:
+        raise MlaAttnError(rc, "mla_attn_append_fwd: ")
+    return out
 
 
 def mla_attn_get_status(workspace: Workspace | None = None, device=None, stream=None) -> int:

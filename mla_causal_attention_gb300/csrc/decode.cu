@@ -138,13 +138,25 @@ __global__ void __launch_bounds__(DecCfg<G, T, NST, WPH>::kThreads, MINB)
         const int nt = min(T, j1 - jt);
         uint8_t* st = stages + slot * C::kStageBytes;
         mbar_arrive_expect_tx(&full[slot], (uint32_t)nt * (128u + (uint32_t)ng * 512u));
-        bulk_g2s(st, p.k_pe + ((size_t)b * p.Tk + jt) * 64, nt * 128, &full[slot], pol_kpe);
+        // With a fused append, the stage holding key row Tk-1 takes that row from the new
+        // token's buffers; the cache supplies the rows before it.
+        const bool subst = p.new_k_nope != nullptr && jt + nt == p.Tk;
+        const int nc = subst ? nt - 1 : nt;  // rows read from the cache
+        if (nc > 0)
+          bulk_g2s(st, p.k_pe + ((size_t)b * p.kv_rows + jt) * 64, nc * 128, &full[slot], pol_kpe);
+        if (subst) bulk_g2s(st + nc * 128, p.new_k_pe + (size_t)b * 64, 128, &full[slot], pol);
         for (int g = 0; g < ng; ++g) {
           const size_t bh = (size_t)b * p.H + h0 + g;
-          bulk_g2s(st + C::kKpeBytes + g * C::kKnBytes, p.k_nope + (bh * p.Tk + jt) * 128,
-                   nt * 256, &full[slot], pol);
-          bulk_g2s(st + C::kKpeBytes + G * C::kKnBytes + g * C::kVBytes,
-                   p.v + (bh * p.Tk + jt) * 128, nt * 256, &full[slot], pol);
+          uint8_t* kn_dst = st + C::kKpeBytes + g * C::kKnBytes;
+          uint8_t* v_dst = st + C::kKpeBytes + G * C::kKnBytes + g * C::kVBytes;
+          if (nc > 0) {
+            bulk_g2s(kn_dst, p.k_nope + (bh * p.kv_rows + jt) * 128, nc * 256, &full[slot], pol);
+            bulk_g2s(v_dst, p.v + (bh * p.kv_rows + jt) * 128, nc * 256, &full[slot], pol);
+          }
+          if (subst) {
+            bulk_g2s(kn_dst + nc * 256, p.new_k_nope + bh * 128, 256, &full[slot], pol);
+            bulk_g2s(v_dst + nc * 256, p.new_v + bh * 128, 256, &full[slot], pol);
+          }
         }
         ++issued;
       }
@@ -173,6 +185,19 @@ __global__ void __launch_bounds__(DecCfg<G, T, NST, WPH>::kThreads, MINB)
     load8(qsrc, p.scale_log2, qn);
     load8(qsrc + 64, p.scale_log2, qn + 8);
     load8(p.q_pe + bh * 64 + l8 * 8, p.scale_log2, qr);
+  }
+
+  // Fused cache append: split 0 of each head group writes the new key/value rows into the
+  // cache (row Tk-1); no CTA of this call reads that cache row.
+  if (p.new_k_nope != nullptr && split == 0 && head_ok && wh == 0 && lane < 16) {
+    const size_t row = bh * p.kv_rows + (p.Tk - 1);
+    reinterpret_cast<uint4*>(p.cache_k_nope + row * 128)[lane] =
+        reinterpret_cast<const uint4*>(p.new_k_nope + bh * 128)[lane];
+    reinterpret_cast<uint4*>(p.cache_v + row * 128)[lane] =
+        reinterpret_cast<const uint4*>(p.new_v + bh * 128)[lane];
+    if (hg == 0 && g == 0 && lane < 8)
+      reinterpret_cast<uint4*>(p.cache_k_pe + ((size_t)b * p.kv_rows + p.Tk - 1) * 64)[lane] =
+          reinterpret_cast<const uint4*>(p.new_k_pe + (size_t)b * 64)[lane];
   }
 
   float m_run = -1e30f;  // finite sentinel: 2^(m_run - m_new) stays defined

@@ -144,16 +144,33 @@ size_t mla_attn_workspace_bytes(int B, int H, int Tq, int Tk) {
   return decode_workspace(B, H, s);
 }
 
-mla_status mla_attn_fwd_ex(const uint16_t* q_nope, const uint16_t* q_pe,
-                           const uint16_t* k_nope, const uint16_t* k_pe_shared,
-                           const uint16_t* v, const int32_t* kv_len, int B, int H, int Tq,
-                           int Tk, int past_len, float softmax_scale, uint16_t* out,
-                           void* workspace, size_t workspace_bytes, void* cuda_stream,
-                           const mla_attn_options* options) {
+}  // extern "C"
+
+namespace mla {
+namespace {
+
+struct AppendPtrs {
+  const uint16_t* new_k_nope;
+  const uint16_t* new_k_pe;
+  const uint16_t* new_v;
+  uint16_t* cache_k_nope;
+  uint16_t* cache_k_pe;
+  uint16_t* cache_v;
+};
+
+// Argument checks and launch shared by mla_attn_fwd_ex and mla_attn_append_fwd.  kv_rows is
+// the row stride of the key/value buffers (>= Tk); app (decode only) fuses the cache append.
+mla_status attention_impl(const uint16_t* q_nope, const uint16_t* q_pe, const uint16_t* k_nope,
+                          const uint16_t* k_pe_shared, const uint16_t* v, const int32_t* kv_len,
+                          int B, int H, int Tq, int Tk, int past_len, float softmax_scale,
+                          uint16_t* out, void* workspace, size_t workspace_bytes,
+                          void* cuda_stream, const mla_attn_options* options, int kv_rows,
+                          const AppendPtrs* app) {
   if (!q_nope || !q_pe || !k_nope || !k_pe_shared || !v || !out) return MLA_ERR_NULL;
   if (!workspace) return MLA_ERR_WORKSPACE;
   mla_status st = check_shape(B, H, Tq, Tk, past_len);
   if (st != MLA_OK) return st;
+  if (kv_rows < Tk || (int64_t)B * H * kv_rows * 128 > kMaxElems) return MLA_ERR_SHAPE;
   if (!aligned16(q_nope) || !aligned16(q_pe) || !aligned16(k_nope) || !aligned16(k_pe_shared) ||
       !aligned16(v) || !aligned16(out) || !aligned16(workspace) ||
       (reinterpret_cast<uintptr_t>(kv_len) & 3u) != 0)
@@ -163,6 +180,7 @@ mla_status mla_attn_fwd_ex(const uint16_t* q_nope, const uint16_t* q_pe,
   if (path < MLA_PATH_AUTO || path > MLA_PATH_DECODE) return MLA_ERR_ARG;
   if (path == MLA_PATH_AUTO) path = (Tq == 1) ? MLA_PATH_DECODE : MLA_PATH_PREFILL;
   if (path == MLA_PATH_DECODE && Tq != 1) return MLA_ERR_ARG;
+  if (app && path != MLA_PATH_DECODE) return MLA_ERR_ARG;
   int sms = 0;
   st = check_device(&sms);
   if (st != MLA_OK) return st;
@@ -180,7 +198,7 @@ mla_status mla_attn_fwd_ex(const uint16_t* q_nope, const uint16_t* q_pe,
     const int chunk = pl.chunk, splits = pl.splits;
     if (splits > 65535) return MLA_ERR_ARG;
     if (workspace_bytes < decode_workspace(B, H, splits)) return MLA_ERR_WORKSPACE;
-    DecodeArgs a;
+    DecodeArgs a{};
     a.q_nope = q_nope; a.q_pe = q_pe; a.k_nope = k_nope; a.k_pe = k_pe_shared; a.v = v;
     a.kv_len = kv_len; a.out = out; a.status = status;
     uint8_t* part = static_cast<uint8_t*>(workspace) + kStatusBytes;
@@ -188,16 +206,86 @@ mla_status mla_attn_fwd_ex(const uint16_t* q_nope, const uint16_t* q_pe,
     a.part_acc = reinterpret_cast<float*>(part + decode_ml_bytes(B, H, splits));
     a.B = B; a.H = H; a.Tk = Tk; a.chunk = chunk; a.splits = splits; a.small = pl.small;
     a.scale_log2 = scale_log2;
+    a.kv_rows = kv_rows;
+    if (app) {
+      a.new_k_nope = app->new_k_nope; a.new_k_pe = app->new_k_pe; a.new_v = app->new_v;
+      a.cache_k_nope = app->cache_k_nope; a.cache_k_pe = app->cache_k_pe;
+      a.cache_v = app->cache_v;
+    }
     return launch_decode(a, stream) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
   }
 
   if (workspace_bytes < kStatusBytes) return MLA_ERR_WORKSPACE;
-  PrefillArgs a;
+  PrefillArgs a{};
   a.q_nope = q_nope; a.q_pe = q_pe; a.k_nope = k_nope; a.k_pe = k_pe_shared; a.v = v;
   a.kv_len = kv_len; a.out = out; a.status = status;
   a.B = B; a.H = H; a.Tq = Tq; a.Tk = Tk; a.past_len = past_len;
   a.scale_log2 = scale_log2;
+  a.kv_rows = kv_rows;
   return launch_prefill(a, stream) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace mla
+
+extern "C" {
+
+mla_status mla_attn_fwd_ex(const uint16_t* q_nope, const uint16_t* q_pe,
+                           const uint16_t* k_nope, const uint16_t* k_pe_shared,
+                           const uint16_t* v, const int32_t* kv_len, int B, int H, int Tq,
+                           int Tk, int past_len, float softmax_scale, uint16_t* out,
+                           void* workspace, size_t workspace_bytes, void* cuda_stream,
+                           const mla_attn_options* options) {
+  return attention_impl(q_nope, q_pe, k_nope, k_pe_shared, v, kv_len, B, H, Tq, Tk, past_len,
+                        softmax_scale, out, workspace, workspace_bytes, cuda_stream, options, Tk,
+                        nullptr);
+}
+
+mla_status mla_attn_append_fwd(const uint16_t* q_nope, const uint16_t* q_pe,
+                               const uint16_t* k_nope_new, const uint16_t* k_pe_new,
+                               const uint16_t* v_new, uint16_t* k_nope_cache,
+                               uint16_t* k_pe_cache, uint16_t* v_cache, const int32_t* kv_len,
+                               int B, int H, int Tq, int T_cap, int past_len,
+                               float softmax_scale, uint16_t* out, void* workspace,
+                               size_t workspace_bytes, void* cuda_stream) {
+  if (!k_nope_new || !k_pe_new || !v_new || !k_nope_cache || !k_pe_cache || !v_cache)
+    return MLA_ERR_NULL;
+  if (B < 1 || H < 1 || Tq < 1 || past_len < 0 || (int64_t)past_len + Tq > (int64_t)T_cap)
+    return MLA_ERR_SHAPE;
+  if (!aligned16(k_nope_new) || !aligned16(k_pe_new) || !aligned16(v_new))
+    return MLA_ERR_ALIGN;
+  const int Tk = past_len + Tq;
+  if (Tq == 1) {
+    // Decode: the append is fused into the attention kernel.
+    AppendPtrs app = {k_nope_new, k_pe_new, v_new, k_nope_cache, k_pe_cache, v_cache};
+    return attention_impl(q_nope, q_pe, k_nope_cache, k_pe_cache, v_cache, kv_len, B, H, Tq, Tk,
+                          past_len, softmax_scale, out, workspace, workspace_bytes, cuda_stream,
+                          nullptr, T_cap, &app);
+  }
+  // Prefill: the checks run first (nothing is enqueued on failure), then the copy kernel
+  // appends the new rows, then attention reads the cache.
+  if (!q_nope || !q_pe || !out) return MLA_ERR_NULL;
+  mla_status st = check_shape(B, H, Tq, Tk, past_len);
+  if (st != MLA_OK) return st;
+  if (!workspace) return MLA_ERR_WORKSPACE;
+  if (workspace_bytes < kStatusBytes) return MLA_ERR_WORKSPACE;
+  if (!aligned16(k_nope_cache) || !aligned16(k_pe_cache) || !aligned16(v_cache) ||
+      !aligned16(q_nope) || !aligned16(q_pe) || !aligned16(out) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(kv_len) & 3u) != 0)
+    return MLA_ERR_ALIGN;
+  if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.0f)) return MLA_ERR_ARG;
+  if ((int64_t)B * H * T_cap * 128 > kMaxElems) return MLA_ERR_SHAPE;
+  st = check_device(nullptr);
+  if (st != MLA_OK) return st;
+  AppendArgs ap;
+  ap.new_k_nope = k_nope_new; ap.new_k_pe = k_pe_new; ap.new_v = v_new;
+  ap.cache_k_nope = k_nope_cache; ap.cache_k_pe = k_pe_cache; ap.cache_v = v_cache;
+  ap.B = B; ap.H = H; ap.Tq = Tq; ap.past_len = past_len; ap.kv_rows = T_cap;
+  if (launch_kv_append(ap, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return attention_impl(q_nope, q_pe, k_nope_cache, k_pe_cache, v_cache, kv_len, B, H, Tq, Tk,
+                        past_len, softmax_scale, out, workspace, workspace_bytes, cuda_stream,
+                        nullptr, T_cap, nullptr);
 }
 
 mla_status mla_attn_fwd(const uint16_t* q_nope, const uint16_t* q_pe, const uint16_t* k_nope,

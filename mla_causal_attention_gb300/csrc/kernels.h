@@ -25,6 +25,16 @@ struct DecodeArgs {
   int splits;  // ceil(Tk / chunk)
   int small;   // 1: 16-key stages, 2 CTAs per SM (problems smaller than one wave)
   float scale_log2;  // softmax_scale * log2(e)
+  int kv_rows;       // rows per (b, h) of k_nope / v and per b of k_pe (>= Tk)
+  // Optional fused cache append (all null otherwise): key row Tk-1 is taken from new_*
+  // ([B,H,1,128], [B,1,64], [B,H,1,128]) instead of the cache, and written into the cache
+  // at row Tk-1 through cache_* (the same buffers as k_nope / k_pe / v).
+  const uint16_t* new_k_nope;
+  const uint16_t* new_k_pe;
+  const uint16_t* new_v;
+  uint16_t* cache_k_nope;
+  uint16_t* cache_k_pe;
+  uint16_t* cache_v;
 };
 
 // Decode kernel configuration (shared with the scheduler).
@@ -55,9 +65,23 @@ struct PrefillArgs {
   int* status;
   int B, H, Tq, Tk, past_len;
   float scale_log2;
+  int kv_rows;  // rows per (b, h) of k_nope / v and per b of k_pe (>= Tk)
 };
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
+
+// Cache append for Tq > 1: new rows [B,H,Tq,128] / [B,Tq,64] / [B,H,Tq,128] are copied to
+// rows [past_len, past_len + Tq) of caches with kv_rows rows per (b, h) (per b for k_pe).
+struct AppendArgs {
+  const uint16_t* new_k_nope;
+  const uint16_t* new_k_pe;
+  const uint16_t* new_v;
+  uint16_t* cache_k_nope;
+  uint16_t* cache_k_pe;
+  uint16_t* cache_v;
+  int B, H, Tq, past_len, kv_rows;
+};
+cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream);
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();

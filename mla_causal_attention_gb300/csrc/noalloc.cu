@@ -81,7 +81,7 @@ extern "C" mla_status mla_attn_decode_noalloc(const uint16_t* q_nope, const uint
   const mla_status st = scratch_for_current_device(&scratch);
   if (st != MLA_OK) return st;
 
-  DecodeArgs a;
+  DecodeArgs a{};
   a.q_nope = q_nope;
   a.q_pe = q_pe;
   a.k_nope = k_nope;
@@ -98,6 +98,7 @@ extern "C" mla_status mla_attn_decode_noalloc(const uint16_t* q_nope, const uint
   a.chunk = chunk;
   a.splits = splits;
   a.small = pl.small;
+  a.kv_rows = Tk;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   return launch_decode(a, static_cast<cudaStream_t>(cuda_stream)) == cudaSuccess ? MLA_OK
                                                                                  : MLA_ERR_CUDA;

@@ -29,6 +29,7 @@
 // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512).
 #include <cuda.h>
 
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 
@@ -503,12 +504,12 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// bf16 tensor viewed as {inner, rows, planes} with 128-byte swizzled {64, 128, 1} boxes;
-// rows past the end of a plane read as zeros.
+// bf16 tensor viewed as {inner, rows, planes} (planes plane_rows rows apart) with 128-byte
+// swizzled {64, 128, 1} boxes; rows past `rows` read as zeros.
 bool encode_3d(EncodeTiledFn fn, CUtensorMap* m, const void* base, uint64_t inner,
-               uint64_t rows, uint64_t planes) {
+               uint64_t rows, uint64_t planes, uint64_t plane_rows) {
   cuuint64_t dims[3] = {inner, rows, planes};
-  cuuint64_t strides[2] = {inner * 2, inner * 2 * rows};
+  cuuint64_t strides[2] = {inner * 2, inner * 2 * plane_rows};
   cuuint32_t box[3] = {64, 128, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
@@ -521,11 +522,11 @@ bool encode_3d(EncodeTiledFn fn, CUtensorMap* m, const void* base, uint64_t inne
 // a serving loop calls the same buffers over and over, and encoding costs microseconds.
 struct MapKey {
   const void* ptr[5];
-  int B, H, Tq, Tk;
+  int B, H, Tq, Tk, kv_rows;
   bool operator==(const MapKey& o) const {
     for (int i = 0; i < 5; ++i)
       if (ptr[i] != o.ptr[i]) return false;
-    return B == o.B && H == o.H && Tq == o.Tq && Tk == o.Tk;
+    return B == o.B && H == o.H && Tq == o.Tq && Tk == o.Tk && kv_rows == o.kv_rows;
   }
 };
 struct MapEntry {
@@ -539,7 +540,7 @@ MapEntry g_map_cache[kMapCacheSize];
 int g_map_next = 0;
 
 bool tensor_maps(const PrefillArgs& a, PrefillParams* p) {
-  const MapKey key = {{a.q_nope, a.q_pe, a.k_nope, a.k_pe, a.v}, a.B, a.H, a.Tq, a.Tk};
+  const MapKey key = {{a.q_nope, a.q_pe, a.k_nope, a.k_pe, a.v}, a.B, a.H, a.Tq, a.Tk, a.kv_rows};
   {
     std::lock_guard<std::mutex> lk(g_map_mu);
     for (const MapEntry& e : g_map_cache) {
@@ -556,11 +557,11 @@ bool tensor_maps(const PrefillArgs& a, PrefillParams* p) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) return false;
   const uint64_t BH = (uint64_t)a.B * a.H;
-  if (!encode_3d(fn, &p->tm_qn, a.q_nope, 128, a.Tq, BH) ||
-      !encode_3d(fn, &p->tm_qr, a.q_pe, 64, a.Tq, BH) ||
-      !encode_3d(fn, &p->tm_kn, a.k_nope, 128, a.Tk, BH) ||
-      !encode_3d(fn, &p->tm_kr, a.k_pe, 64, a.Tk, a.B) ||
-      !encode_3d(fn, &p->tm_v, a.v, 128, a.Tk, BH))
+  if (!encode_3d(fn, &p->tm_qn, a.q_nope, 128, a.Tq, BH, a.Tq) ||
+      !encode_3d(fn, &p->tm_qr, a.q_pe, 64, a.Tq, BH, a.Tq) ||
+      !encode_3d(fn, &p->tm_kn, a.k_nope, 128, a.Tk, BH, a.kv_rows) ||
+      !encode_3d(fn, &p->tm_kr, a.k_pe, 64, a.Tk, a.B, a.kv_rows) ||
+      !encode_3d(fn, &p->tm_v, a.v, 128, a.Tk, BH, a.kv_rows))
     return false;
   std::lock_guard<std::mutex> lk(g_map_mu);
   MapEntry& e = g_map_cache[g_map_next];
@@ -576,6 +577,42 @@ bool tensor_maps(const PrefillArgs& a, PrefillParams* p) {
 }
 
 }  // namespace
+
+// Cache append for Tq > 1 (the cache update of the attention excerpt: the new rows follow
+// the cached prefix).  One thread per 16-byte chunk; rows of k_nope / v are 16 chunks, rows
+// of the shared rotary key 8.
+__global__ void __launch_bounds__(256) kv_append_kernel(const AppendArgs a) {
+  const size_t bh_rows = (size_t)a.B * a.H * a.Tq;  // k_nope and v rows
+  const size_t pe_rows = (size_t)a.B * a.Tq;        // k_pe rows
+  const size_t n16 = bh_rows * 16 * 2 + pe_rows * 8;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16;
+       i += (size_t)gridDim.x * blockDim.x) {
+    if (i < bh_rows * 32) {
+      const bool is_v = i >= bh_rows * 16;
+      const size_t k = is_v ? i - bh_rows * 16 : i;
+      const size_t row = k >> 4, c = k & 15;      // row = (b*H + h)*Tq + t
+      const size_t bh = row / a.Tq, t = row % a.Tq;
+      const uint4* src = reinterpret_cast<const uint4*>((is_v ? a.new_v : a.new_k_nope) + row * 128);
+      uint4* dst = reinterpret_cast<uint4*>((is_v ? a.cache_v : a.cache_k_nope) +
+                                            (bh * a.kv_rows + a.past_len + t) * 128);
+      dst[c] = src[c];
+    } else {
+      const size_t k = i - bh_rows * 32;
+      const size_t row = k >> 3, c = k & 7;       // row = b*Tq + t
+      const size_t b = row / a.Tq, t = row % a.Tq;
+      reinterpret_cast<uint4*>(a.cache_k_pe + (b * a.kv_rows + a.past_len + t) * 64)[c] =
+          reinterpret_cast<const uint4*>(a.new_k_pe + row * 64)[c];
+    }
+  }
+}
+
+cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream) {
+  const size_t n16 = (size_t)a.B * a.H * a.Tq * 32 + (size_t)a.B * a.Tq * 8;
+  const int sms = device_sm_count();
+  const size_t blocks = std::min<size_t>((n16 + 255) / 256, (size_t)(sms > 0 ? sms : 152) * 8);
+  kv_append_kernel<<<(unsigned)std::max<size_t>(blocks, 1), 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   PrefillParams p;
