@@ -320,22 +320,44 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeArgs p)
   kvl = min(max(kvl, 1), p.Tk);
   const int n = (kvl + p.chunk - 1) / p.chunk;
   const size_t base = (size_t)w * p.splits;
+  // (max, sum) of up to 32 splits per pass, one split per lane, loaded in parallel; then
+  // the 128-column accumulators in batches of 8 independent loads per lane, so a merge
+  // costs a few memory round trips instead of one per split.
   float m = -1e30f;
   for (int s = lane; s < n; s += 32) m = fmaxf(m, p.part_ml[(base + s) * 2]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   float l = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = 0; s < n; ++s) {
-    const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + (base + s) * 2);
-    const float f = ex2_approx(ml.x - m);
-    l += f * ml.y;
-    const float4 a = *reinterpret_cast<const float4*>(p.part_acc + (base + s) * 128 + lane * 4);
-    acc.x += f * a.x;
-    acc.y += f * a.y;
-    acc.z += f * a.z;
-    acc.w += f * a.w;
+  for (int s0 = 0; s0 < n; s0 += 32) {
+    float f = 0.f;  // this lane's split weight 2^(m_s - m)
+    if (s0 + lane < n) {
+      const float2 ml = *reinterpret_cast<const float2*>(p.part_ml + (base + s0 + lane) * 2);
+      f = ex2_approx(ml.x - m);
+      l += f * ml.y;
+    }
+    const int cnt = min(32, n - s0);
+    for (int s1 = 0; s1 < cnt; s1 += 8) {
+      float4 a[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (s1 + k < cnt)
+          a[k] = *reinterpret_cast<const float4*>(p.part_acc + (base + s0 + s1 + k) * 128 +
+                                                  lane * 4);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float fk = __shfl_sync(0xffffffffu, f, s1 + k);
+        if (s1 + k < cnt) {
+          acc.x += fk * a[k].x;
+          acc.y += fk * a[k].y;
+          acc.z += fk * a[k].z;
+          acc.w += fk * a[k].w;
+        }
+      }
+    }
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
   const float inv = 1.f / l;
   uint2 o;
   o.x = pack_bf16x2(acc.x * inv, acc.y * inv);
