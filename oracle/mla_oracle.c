@@ -87,12 +87,27 @@ typedef struct {
   const int64_t* rows;
   int64_t n_rows;
   int mode;
+  const double* rope_inv_freq; /* NULL: inputs already rotated; else 32 frequencies */
+  double rope_mscale;
   double* out;
   double* wsum;
   int64_t next; /* shared work counter, guarded by lock */
   pthread_mutex_t lock;
   int err;
 } job_t;
+
+/* Rotary embedding of the 64 rotary columns at position pos (rotate-half form):
+ *   y[d]      = x[d]      cos(pos f_d) - x[d + 32] sin(pos f_d)
+ *   y[d + 32] = x[d + 32] cos(pos f_d) + x[d]      sin(pos f_d),   d < 32,
+ * with cos and sin multiplied by the YaRN mscale ratio. */
+static void rotate64(double* y, const double* x, double pos, const double* f, double msc) {
+  for (int d = 0; d < 32; ++d) {
+    const double a = pos * f[d];
+    const double c = cos(a) * msc, sn = sin(a) * msc;
+    y[d] = x[d] * c - x[d + 32] * sn;
+    y[d + 32] = x[d + 32] * c + x[d] * sn;
+  }
+}
 
 /* One output row o[b, h, i, :].  s is scratch of Tk doubles. */
 static int one_row(const job_t* J, int64_t flat, double* s, double* o, double* wsum_out) {
@@ -110,6 +125,12 @@ static int one_row(const job_t* J, int64_t flat, double* s, double* o, double* w
   const uint16_t* qr = J->q_pe + (bh * J->Tq + i) * D_ROPE;
   for (int d = 0; d < D_NOPE; ++d) q[d] = bf16_to_double(qn[d]);
   for (int d = 0; d < D_ROPE; ++d) q[D_NOPE + d] = bf16_to_double(qr[d]);
+  if (J->rope_inv_freq) {
+    /* The query's rotary part arrives unrotated; query i sits at position past_len + i. */
+    double raw[D_ROPE];
+    for (int d = 0; d < D_ROPE; ++d) raw[d] = q[D_NOPE + d];
+    rotate64(q + D_NOPE, raw, (double)(J->past_len + i), J->rope_inv_freq, J->rope_mscale);
+  }
 
   /* The scale is a Python float multiplied into a bf16 tensor: eager computes the product
    * with the scale as an fp32 value, which is what J->scale holds in both modes. */
@@ -121,7 +142,16 @@ static int one_row(const job_t* J, int64_t flat, double* s, double* o, double* w
     /* Step 3: dot product over all 192 columns, then the scale. */
     double acc = 0.0;
     for (int d = 0; d < D_NOPE; ++d) acc += q[d] * bf16_to_double(kn[d]);
-    for (int d = 0; d < D_ROPE; ++d) acc += q[D_NOPE + d] * bf16_to_double(kr[d]);
+    if (J->rope_inv_freq && j >= J->past_len) {
+      /* A new key's rotary part arrives unrotated and is rotated at its position j; the
+       * cached rows (j < past_len) were stored rotated. */
+      double raw[D_ROPE], rot[D_ROPE];
+      for (int d = 0; d < D_ROPE; ++d) raw[d] = bf16_to_double(kr[d]);
+      rotate64(rot, raw, (double)j, J->rope_inv_freq, J->rope_mscale);
+      for (int d = 0; d < D_ROPE; ++d) acc += q[D_NOPE + d] * rot[d];
+    } else {
+      for (int d = 0; d < D_ROPE; ++d) acc += q[D_NOPE + d] * bf16_to_double(kr[d]);
+    }
     if (eager) acc = round_bf16(acc);
     double sj = acc * scale_used;
     if (eager) sj = round_bf16(sj);
@@ -201,11 +231,11 @@ static void* worker(void* arg) {
  *   out [n_rows,128] and wsum [n_rows] (may be NULL): written as double.
  * Returns 0, or a nonzero code for bad arguments (shape, kv_len out of [1,Tk], alloc).
  */
-int mla_oracle_rows(const uint16_t* q_nope, const uint16_t* q_pe, const uint16_t* k_nope,
-                    const uint16_t* k_pe, const uint16_t* v, const int32_t* kv_len, int64_t B,
-                    int64_t H, int64_t Tq, int64_t Tk, int64_t past_len, float softmax_scale,
-                    const int64_t* rows, int64_t n_rows, int mode, int nthreads, double* out,
-                    double* wsum) {
+static int rows_impl(const uint16_t* q_nope, const uint16_t* q_pe, const uint16_t* k_nope,
+                     const uint16_t* k_pe, const uint16_t* v, const int32_t* kv_len, int64_t B,
+                     int64_t H, int64_t Tq, int64_t Tk, int64_t past_len, float softmax_scale,
+                     const int64_t* rows, int64_t n_rows, int mode, int nthreads, double* out,
+                     double* wsum, const double* rope_inv_freq, double rope_mscale) {
   if (B < 1 || H < 1 || Tq < 1 || Tk < 1 || past_len < 0 || Tk != past_len + Tq) return 10;
   if (!q_nope || !q_pe || !k_nope || !k_pe || !v || !out) return 11;
   if (mode != 0 && mode != 1) return 12;
@@ -222,6 +252,8 @@ int mla_oracle_rows(const uint16_t* q_nope, const uint16_t* q_pe, const uint16_t
   J.B = B; J.H = H; J.Tq = Tq; J.Tk = Tk; J.past_len = past_len;
   J.scale = (double)softmax_scale;
   J.rows = rows; J.n_rows = n_rows; J.mode = mode; J.out = out; J.wsum = wsum;
+  J.rope_inv_freq = rope_inv_freq;
+  J.rope_mscale = rope_mscale;
   pthread_mutex_init(&J.lock, NULL);
   if (nthreads < 1) nthreads = 1;
   if (nthreads > 256) nthreads = 256;
@@ -233,6 +265,67 @@ int mla_oracle_rows(const uint16_t* q_nope, const uint16_t* q_pe, const uint16_t
   for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
   pthread_mutex_destroy(&J.lock);
   return J.err;
+}
+
+int mla_oracle_rows(const uint16_t* q_nope, const uint16_t* q_pe, const uint16_t* k_nope,
+                    const uint16_t* k_pe, const uint16_t* v, const int32_t* kv_len, int64_t B,
+                    int64_t H, int64_t Tq, int64_t Tk, int64_t past_len, float softmax_scale,
+                    const int64_t* rows, int64_t n_rows, int mode, int nthreads, double* out,
+                    double* wsum) {
+  return rows_impl(q_nope, q_pe, k_nope, k_pe, v, kv_len, B, H, Tq, Tk, past_len, softmax_scale,
+                   rows, n_rows, mode, nthreads, out, wsum, NULL, 1.0);
+}
+
+/*
+ * The same rows with the rotary step of the attention excerpt applied first
+ * ("q_pe, k_pe = apply_rotary_pos_emb(q_pe, k_pe, cos, sin, position_ids)"): q_pe holds
+ * unrotated query rows (query i at position past_len + i); k_pe rows j >= past_len hold
+ * unrotated new keys (rotated at position j); rows j < past_len are cached, already rotated.
+ * inv_freq: the 32 rotary frequencies; mscale: factor on cos and sin.
+ */
+int mla_oracle_rows_rope(const uint16_t* q_nope, const uint16_t* q_pe, const uint16_t* k_nope,
+                         const uint16_t* k_pe, const uint16_t* v, const int32_t* kv_len,
+                         int64_t B, int64_t H, int64_t Tq, int64_t Tk, int64_t past_len,
+                         float softmax_scale, const int64_t* rows, int64_t n_rows, int nthreads,
+                         double* out, const double* inv_freq, double mscale) {
+  if (!inv_freq) return 14;
+  return rows_impl(q_nope, q_pe, k_nope, k_pe, v, kv_len, B, H, Tq, Tk, past_len, softmax_scale,
+                   rows, n_rows, 0, nthreads, out, NULL, inv_freq, mscale);
+}
+
+/*
+ * YaRN rotary frequencies for a 64-column rotary part (Peng et al., "YaRN: Efficient
+ * Context Window Extension of Large Language Models", 2023), as configured by the
+ * rope_scaling block of the config.json excerpt on "Kimi K2 · Logits":
+ *   extrapolated f_d = theta^(-2d/64), interpolated f_d / factor;
+ *   the dimension at which a wavelength makes n rotations over the original context L is
+ *     dim(n) = 64 ln(L / (2 pi n)) / (2 ln theta);
+ *   low = floor(dim(beta_fast)), high = ceil(dim(beta_slow)), clamped to [0, 31];
+ *   ramp_d = clamp((d - low) / (high - low), 0, 1)  (high == low: high + 0.001);
+ *   f_d = interpolated * ramp_d + extrapolated * (1 - ramp_d).
+ * Returns through mscale_ratio the factor on cos and sin,
+ *   m(factor, mscale) / m(factor, mscale_all_dim),  m(s, k) = 0.1 k ln s + 1 (s > 1), else 1.
+ */
+void mla_oracle_yarn(double theta, double factor, double orig_max_pos, double beta_fast,
+                     double beta_slow, double mscale, double mscale_all_dim, double* inv_freq,
+                     double* mscale_ratio) {
+  const double pi = 3.14159265358979323846;
+  double low = floor(64.0 * log(orig_max_pos / (2.0 * pi * beta_fast)) / (2.0 * log(theta)));
+  double high = ceil(64.0 * log(orig_max_pos / (2.0 * pi * beta_slow)) / (2.0 * log(theta)));
+  if (low < 0.0) low = 0.0;
+  if (high > 31.0) high = 31.0;
+  if (high == low) high += 0.001;
+  for (int d = 0; d < 32; ++d) {
+    const double extra = pow(theta, -2.0 * d / 64.0);
+    const double inter = extra / factor;
+    double ramp = ((double)d - low) / (high - low);
+    if (ramp < 0.0) ramp = 0.0;
+    if (ramp > 1.0) ramp = 1.0;
+    inv_freq[d] = inter * ramp + extra * (1.0 - ramp);
+  }
+  const double m1 = factor > 1.0 ? 0.1 * mscale * log(factor) + 1.0 : 1.0;
+  const double m2 = factor > 1.0 ? 0.1 * mscale_all_dim * log(factor) + 1.0 : 1.0;
+  *mscale_ratio = m1 / m2;
 }
 
 /* Exposed for the test that pins the diagnostic rounding against torch's own cast. */

@@ -60,6 +60,13 @@ def _load():
                                             p, p]
             lib.mla_oracle_round_bf16.restype = ctypes.c_double
             lib.mla_oracle_round_bf16.argtypes = [ctypes.c_double]
+            lib.mla_oracle_rows_rope.restype = ctypes.c_int
+            lib.mla_oracle_rows_rope.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, i64,
+                                                 ctypes.c_float, p, i64, ctypes.c_int, p, p,
+                                                 ctypes.c_double]
+            d = ctypes.c_double
+            lib.mla_oracle_yarn.restype = None
+            lib.mla_oracle_yarn.argtypes = [d, d, d, d, d, d, d, p, p]
             _lib = lib
     return _lib
 
@@ -133,3 +140,41 @@ def oracle_full(inp: dict, mode: str = "exact", threads: int | None = None) -> n
 def round_bf16(x: float) -> float:
     """The eager-emulation diagnostic's round-to-bf16 (exposed so a test can pin it)."""
     return _load().mla_oracle_round_bf16(float(x))
+
+
+def yarn(theta: float, factor: float, orig_max_pos: int, beta_fast: float, beta_slow: float,
+         mscale: float, mscale_all_dim: float):
+    """The 32 YaRN rotary frequencies and the mscale ratio on cos/sin (fp64)."""
+    lib = _load()
+    f = np.zeros(32, dtype=np.float64)
+    r = np.zeros(1, dtype=np.float64)
+    lib.mla_oracle_yarn(float(theta), float(factor), float(orig_max_pos), float(beta_fast),
+                        float(beta_slow), float(mscale), float(mscale_all_dim), f.ctypes.data,
+                        r.ctypes.data)
+    return f, float(r[0])
+
+
+def oracle_rows_rope(q_nope, q_pe_raw, k_nope, k_pe, v, kv_len, past_len: int,
+                     softmax_scale: float, inv_freq, mscale: float, rows=None,
+                     threads: int | None = None):
+    """Like oracle_rows, with the rotary step first: q_pe_raw unrotated (query i at position
+    past_len + i); k_pe rows j >= past_len unrotated new keys (position j); rows below
+    past_len are cached keys, already rotated."""
+    lib = _load()
+    qn, qr, kn, kr, vv = (_bits(t) for t in (q_nope, q_pe_raw, k_nope, k_pe, v))
+    B, H, Tq, _ = qn.shape
+    Tk = kn.shape[2]
+    kvl = None if kv_len is None else np.ascontiguousarray(
+        np.asarray(kv_len, dtype=np.int32).reshape(B))
+    rows_arr = None if rows is None else np.ascontiguousarray(
+        np.asarray(rows, dtype=np.int64).reshape(-1))
+    n = B * H * Tq if rows is None else rows_arr.size
+    out = np.empty((n, 128), dtype=np.float64)
+    f = np.ascontiguousarray(np.asarray(inv_freq, dtype=np.float64).reshape(32))
+    ptr = lambda a: None if a is None else a.ctypes.data  # noqa: E731
+    rc = lib.mla_oracle_rows_rope(ptr(qn), ptr(qr), ptr(kn), ptr(kr), ptr(vv), ptr(kvl), B, H,
+                                  Tq, Tk, int(past_len), float(softmax_scale), ptr(rows_arr), n,
+                                  _threads(threads), ptr(out), ptr(f), float(mscale))
+    if rc != 0:
+        raise ValueError(f"oracle rejected its arguments (code {rc})")
+    return out

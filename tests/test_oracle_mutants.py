@@ -29,10 +29,23 @@ MUTANTS = {
 }
 
 
-@pytest.mark.parametrize("name", sorted(MUTANTS))
-def test_pins_kill_mutant(name, tmp_path):
+# Mistakes in the rotary step, checked against the rotary pins.
+ROPE_MUTANTS = {
+    "rope_query_position_ignores_past": (
+        "rotate64(q + D_NOPE, raw, (double)(J->past_len + i),",
+        "rotate64(q + D_NOPE, raw, (double)(i),"),
+    "rope_cached_keys_rotated_again": ("if (J->rope_inv_freq && j >= J->past_len) {",
+                                       "if (J->rope_inv_freq) {"),
+    "rope_sine_sign": ("y[d] = x[d] * c - x[d + 32] * sn;", "y[d] = x[d] * c + x[d + 32] * sn;"),
+    "rope_ramp_inverted": ("inv_freq[d] = inter * ramp + extra * (1.0 - ramp);",
+                           "inv_freq[d] = extra * ramp + inter * (1.0 - ramp);"),
+    "rope_pairs_adjacent": ("y[d + 32] = x[d + 32] * c + x[d] * sn;",
+                            "y[d + 32] = x[d + 32] * c + x[(d + 1) & 31] * sn;"),
+}
+
+
+def _run_pins(name, old, new, tmp_path, pin_file):
     src = open(SRC).read()
-    old, new = MUTANTS[name]
     assert old in src, f"mutation site for {name} not found"
     mut = tmp_path / "mut.c"
     mut.write_text(src.replace(old, new))
@@ -40,7 +53,19 @@ def test_pins_kill_mutant(name, tmp_path):
     subprocess.run(["gcc", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-pthread", "-o",
                     str(lib), str(mut), "-lm"], check=True)
     env = dict(os.environ, MLA_ORACLE_LIB=str(lib))
-    r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(ROOT, "tests",
-                        "test_oracle.py"), "-q", "-x", "-p", "no:cacheprovider"],
+    r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(ROOT, "tests", pin_file),
+                        "-q", "-x", "-p", "no:cacheprovider"],
                        capture_output=True, text=True, env=env, cwd=ROOT, timeout=300)
     assert r.returncode == 1, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_kill_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    _run_pins(name, old, new, tmp_path, "test_oracle.py")
+
+
+@pytest.mark.parametrize("name", sorted(ROPE_MUTANTS))
+def test_rope_pins_kill_mutant(name, tmp_path):
+    old, new = ROPE_MUTANTS[name]
+    _run_pins(name, old, new, tmp_path, "test_oracle_rope.py")
