@@ -157,6 +157,81 @@ MLA_API mla_status mla_attn_append_fwd(const uint16_t* q_nope, const uint16_t* q
                                        void* cuda_stream);
 
 /*
+ * Rotary embedding.  The attention excerpt on "Kimi K2 · Similarities" rotates the query's
+ * and the new keys' rotary parts before the cache update (rotary_emb gives cos and sin for
+ * the positions, apply_rotary_pos_emb rotates q_pe and k_pe), and the rope_scaling block of
+ * the config.json excerpt on "Kimi K2 · Logits" selects YaRN scaling (Peng et al., "YaRN:
+ * Efficient Context Window Extension of Large Language Models", 2023).  The pages give the
+ * calls and the configuration, not the function bodies; the library takes the published
+ * YaRN method:
+ *   extrapolated f_d = theta^(-2d/64), interpolated f_d / factor   (d = 0..31)
+ *   dim(n) = 64 ln(L / (2 pi n)) / (2 ln theta)   (L = original_max_position)
+ *   low = floor(dim(beta_fast)), high = ceil(dim(beta_slow)), clamped to [0, 31]
+ *   ramp_d = clamp((d - low) / (high - low), 0, 1)   (high == low: high + 0.001)
+ *   f_d = interpolated * ramp_d + extrapolated * (1 - ramp_d)
+ *   mscale ratio = m(factor, mscale) / m(factor, mscale_all_dim),
+ *                  m(s, k) = 0.1 k ln s + 1 for s > 1, else 1
+ * and the rotate-half rotation of the 64 rotary columns of a row at position p:
+ *   y[d]    = x[d]    * c - x[d+32] * s
+ *   y[d+32] = x[d+32] * c + x[d]    * s,     c = cos(p f_d) * ratio, s = sin(p f_d) * ratio
+ * Kimi K2's values: theta 50000, factor 32, original_max_position 4096, beta_fast 1,
+ * beta_slow 1, mscale 1, mscale_all_dim 1.
+ */
+typedef struct {
+  double rope_theta;            /* > 1 */
+  double factor;                /* >= 1 */
+  double original_max_position; /* > 0 */
+  double beta_fast;             /* >= beta_slow */
+  double beta_slow;             /* > 0 */
+  double mscale;
+  double mscale_all_dim;
+} mla_rope_config;
+
+/*
+ * Host only: the 32 frequencies f_d and the mscale ratio of a configuration (written
+ * through the non-NULL pointers).  MLA_ERR_NULL without cfg; MLA_ERR_ARG for values out of
+ * the ranges above or not finite.
+ */
+MLA_API mla_status mla_rope_frequencies(const mla_rope_config* cfg, double* inv_freq,
+                                        double* mscale_ratio);
+
+/*
+ * Fills table (device, float, [max_pos][64], 16-byte aligned) with cos(p f_d) * ratio in
+ * columns 0..31 and sin(p f_d) * ratio in columns 32..63 for positions p < max_pos; the
+ * angles are formed and evaluated in double, then rounded to float.  Build it once per
+ * configuration and pass it to mla_attn_rope_append_fwd.  Enqueued on cuda_stream.
+ */
+MLA_API mla_status mla_rope_table(const mla_rope_config* cfg, int max_pos, float* table,
+                                  void* cuda_stream);
+
+/* Bytes of workspace mla_attn_rope_append_fwd needs (0 for invalid sizes). */
+MLA_API size_t mla_attn_rope_workspace_bytes(int B, int H, int Tq, int Tk);
+
+/*
+ * Rotary step + cache append + attention.  As mla_attn_append_fwd, except that q_pe_raw
+ * and k_pe_new_raw arrive unrotated: query t and new key t are rotated at position
+ * past_len + t with the table from mla_rope_table (table_rows >= past_len + Tq rows, else
+ * MLA_ERR_SHAPE); the rotated new keys are what the k_pe cache receives (cached rows are
+ * stored rotated and are not rotated again); the rotated queries are kept in the
+ * workspace (at least mla_attn_rope_workspace_bytes(B, H, Tq, past_len + Tq) bytes, zeroed
+ * once like mla_attn_fwd's).  Rotated values are rounded to bf16, the type of the cache.
+ * With Tq == 1 one small kernel rotates the query and the new rotary key into the
+ * workspace and the decode kernel appends the new rows to the cache; with Tq > 1 one
+ * kernel rotates the query, rotates and appends the rotary keys and appends the no-rope key
+ * and value rows, then the prefill kernel runs.  All host checks run before anything is
+ * enqueued.
+ */
+MLA_API mla_status mla_attn_rope_append_fwd(const uint16_t* q_nope, const uint16_t* q_pe_raw,
+                                            const uint16_t* k_nope_new,
+                                            const uint16_t* k_pe_new_raw, const uint16_t* v_new,
+                                            uint16_t* k_nope_cache, uint16_t* k_pe_cache,
+                                            uint16_t* v_cache, const int32_t* kv_len, int B,
+                                            int H, int Tq, int T_cap, int past_len,
+                                            float softmax_scale, const float* rope_table,
+                                            int table_rows, uint16_t* out, void* workspace,
+                                            size_t workspace_bytes, void* cuda_stream);
+
+/*
  * Synchronises cuda_stream, reads the device status word in the workspace, clears it,
  * and returns it (MLA_OK if no kernel recorded a problem since the last read).
  */

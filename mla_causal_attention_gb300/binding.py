@@ -42,6 +42,20 @@ class MlaAttnError(RuntimeError):
         super().__init__(f"{msg}{self.status!r}: {_status_string(status)}")
 
 
+class RopeConfig(ctypes.Structure):
+    """mla_rope_config: YaRN rotary scaling (Kimi K2's values are the defaults)."""
+    _fields_ = [("rope_theta", ctypes.c_double), ("factor", ctypes.c_double),
+                ("original_max_position", ctypes.c_double), ("beta_fast", ctypes.c_double),
+                ("beta_slow", ctypes.c_double), ("mscale", ctypes.c_double),
+                ("mscale_all_dim", ctypes.c_double)]
+
+    def __init__(self, rope_theta=50000.0, factor=32.0, original_max_position=4096,
+                 beta_fast=1.0, beta_slow=1.0, mscale=1.0, mscale_all_dim=1.0):
+        super().__init__(float(rope_theta), float(factor), float(original_max_position),
+                         float(beta_fast), float(beta_slow), float(mscale),
+                         float(mscale_all_dim))
+
+
 class _Options(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int), ("decode_chunk", ctypes.c_int),
                 ("reserved", ctypes.c_int * 6)]
@@ -49,7 +63,8 @@ class _Options(ctypes.Structure):
 
 EXPORTED = ("mla_attn_workspace_bytes", "mla_attn_fwd", "mla_attn_fwd_ex",
             "mla_attn_get_status", "mla_status_string", "mla_attn_decode_plan",
-            "mla_attn_append_fwd")
+            "mla_attn_append_fwd", "mla_rope_frequencies", "mla_rope_table",
+            "mla_attn_rope_workspace_bytes", "mla_attn_rope_append_fwd")
 
 
 def library():
@@ -80,6 +95,17 @@ def library():
         lib.mla_attn_append_fwd.restype = i
         lib.mla_attn_append_fwd.argtypes = [p, p, p, p, p, p, p, p, p, i, i, i, i, i, f, p, p,
                                             sz, p]
+        lib.mla_rope_frequencies.restype = i
+        lib.mla_rope_frequencies.argtypes = [ctypes.POINTER(RopeConfig),
+                                             ctypes.POINTER(ctypes.c_double),
+                                             ctypes.POINTER(ctypes.c_double)]
+        lib.mla_rope_table.restype = i
+        lib.mla_rope_table.argtypes = [ctypes.POINTER(RopeConfig), i, p, p]
+        lib.mla_attn_rope_workspace_bytes.restype = sz
+        lib.mla_attn_rope_workspace_bytes.argtypes = [i, i, i, i]
+        lib.mla_attn_rope_append_fwd.restype = i
+        lib.mla_attn_rope_append_fwd.argtypes = [p, p, p, p, p, p, p, p, p, i, i, i, i, i, f,
+                                                 p, i, p, p, sz, p]
         _lib = lib
         return lib
 
@@ -239,6 +265,73 @@ def mla_attn_append_fwd(q_nope, q_pe, k_nope_new, k_pe_new, v_new, k_nope_cache,
                                      _ptr(ws), ws.numel(), ctypes.c_void_p(s.cuda_stream))
     if rc != 0:
         raise MlaAttnError(rc, "mla_attn_append_fwd: ")
+    return out
+
+
+def mla_rope_frequencies(cfg: RopeConfig | None = None):
+    """(inv_freq[32] as a list of floats, mscale ratio) computed by the library's host code."""
+    cfg = cfg or RopeConfig()
+    f = (ctypes.c_double * 32)()
+    m = ctypes.c_double()
+    rc = library().mla_rope_frequencies(ctypes.byref(cfg), f, ctypes.byref(m))
+    if rc != 0:
+        raise MlaAttnError(rc, "mla_rope_frequencies: ")
+    return list(f), m.value
+
+
+def mla_rope_table(max_pos: int, cfg: RopeConfig | None = None, device=None, stream=None):
+    """Device float32 [max_pos, 64] cos|sin table (times the mscale ratio)."""
+    cfg = cfg or RopeConfig()
+    dev = torch.device(device or "cuda")
+    table = torch.empty((max_pos, 64), dtype=torch.float32, device=dev)
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        rc = library().mla_rope_table(ctypes.byref(cfg), int(max_pos), _ptr(table),
+                                      ctypes.c_void_p(s.cuda_stream))
+    if rc != 0:
+        raise MlaAttnError(rc, "mla_rope_table: ")
+    return table
+
+
+def mla_attn_rope_append_fwd(q_nope, q_pe_raw, k_nope_new, k_pe_new_raw, v_new, k_nope_cache,
+                             k_pe_cache, v_cache, kv_len, past_len: int, softmax_scale: float,
+                             rope_table, out=None, workspace: "Workspace | None" = None,
+                             stream=None):
+    """Rotate q_pe_raw / k_pe_new_raw at positions past_len + t (table from mla_rope_table),
+    append the new rows (rotated rotary keys) at [past_len, past_len + Tq) of the caches,
+    then attend over rows [0, past_len + Tq)."""
+    lib = library()
+    dev = q_nope.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    B, H, Tq = q_nope.shape[:3]
+    T_cap = k_nope_cache.shape[2]
+    bf = torch.bfloat16
+    _check(q_nope, "q_nope", bf, (B, H, Tq, 128), dev)
+    _check(q_pe_raw, "q_pe_raw", bf, (B, H, Tq, 64), dev)
+    _check(k_nope_new, "k_nope_new", bf, (B, H, Tq, 128), dev)
+    _check(k_pe_new_raw, "k_pe_new_raw", bf, (B, Tq, 64), dev)
+    _check(v_new, "v_new", bf, (B, H, Tq, 128), dev)
+    _check(k_nope_cache, "k_nope_cache", bf, (B, H, T_cap, 128), dev)
+    _check(k_pe_cache, "k_pe_cache", bf, (B, T_cap, 64), dev)
+    _check(v_cache, "v_cache", bf, (B, H, T_cap, 128), dev)
+    _check(rope_table, "rope_table", torch.float32, (rope_table.shape[0], 64), dev)
+    if kv_len is not None:
+        _check(kv_len, "kv_len", torch.int32, (B,), dev)
+    if out is None:
+        out = torch.empty((B, H, Tq, 128), dtype=bf, device=dev)
+    _check(out, "out", bf, (B, H, Tq, 128), dev)
+    ws = (workspace or _default_workspace(dev)).get(
+        lib.mla_attn_rope_workspace_bytes(B, H, Tq, past_len + Tq))
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        rc = lib.mla_attn_rope_append_fwd(
+            _ptr(q_nope), _ptr(q_pe_raw), _ptr(k_nope_new), _ptr(k_pe_new_raw), _ptr(v_new),
+            _ptr(k_nope_cache), _ptr(k_pe_cache), _ptr(v_cache), _ptr(kv_len), B, H, Tq, T_cap,
+            int(past_len), float(softmax_scale), _ptr(rope_table), int(rope_table.shape[0]),
+            _ptr(out), _ptr(ws), ws.numel(), ctypes.c_void_p(s.cuda_stream))
+    if rc != 0:
+        raise MlaAttnError(rc, "mla_attn_rope_append_fwd: ")
     return out
 
 

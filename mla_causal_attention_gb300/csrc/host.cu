@@ -68,6 +68,26 @@ size_t decode_workspace(int B, int H, int splits) {
          (size_t)B * H * splits * 128 * sizeof(float);
 }
 
+// Rotary workspace: rotated queries [B,H,Tq,64] then rotated new rotary keys [B,Tq,64],
+// each on a 256-byte boundary, after the attention call's own workspace.
+size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+size_t q_rot_bytes(int B, int H, int Tq) { return round256((size_t)B * H * Tq * 64 * 2); }
+size_t rope_bytes(int B, int H, int Tq) {
+  return q_rot_bytes(B, H, Tq) + round256((size_t)B * Tq * 64 * 2);
+}
+
+bool rope_config_ok(const mla_rope_config& c) {
+  const double v[7] = {c.rope_theta, c.factor, c.original_max_position, c.beta_fast,
+                       c.beta_slow, c.mscale, c.mscale_all_dim};
+  for (double x : v)
+    if (!std::isfinite(x)) return false;
+  if (!(c.rope_theta > 1.0 && c.factor >= 1.0 && c.original_max_position > 0.0 &&
+        c.beta_slow > 0.0 && c.beta_fast >= c.beta_slow))
+    return false;
+  // the ratio's denominator 0.1 mscale_all_dim ln(factor) + 1 must not vanish
+  return c.factor == 1.0 || 0.1 * c.mscale_all_dim * std::log(c.factor) + 1.0 != 0.0;
+}
+
 }  // namespace
 
 // Keys per split for the decode path.  When there are at least as many (sequence, head
@@ -158,14 +178,15 @@ struct AppendPtrs {
   uint16_t* cache_v;
 };
 
-// Argument checks and launch shared by mla_attn_fwd_ex and mla_attn_append_fwd.  kv_rows is
-// the row stride of the key/value buffers (>= Tk); app (decode only) fuses the cache append.
+// Argument checks and launch shared by the attention entry points.  kv_rows is the row
+// stride of the key/value buffers (>= Tk); app (decode only) fuses the cache append;
+// check_only runs every check and returns without launching.
 mla_status attention_impl(const uint16_t* q_nope, const uint16_t* q_pe, const uint16_t* k_nope,
                           const uint16_t* k_pe_shared, const uint16_t* v, const int32_t* kv_len,
                           int B, int H, int Tq, int Tk, int past_len, float softmax_scale,
                           uint16_t* out, void* workspace, size_t workspace_bytes,
                           void* cuda_stream, const mla_attn_options* options, int kv_rows,
-                          const AppendPtrs* app) {
+                          const AppendPtrs* app, bool check_only = false) {
   if (!q_nope || !q_pe || !k_nope || !k_pe_shared || !v || !out) return MLA_ERR_NULL;
   if (!workspace) return MLA_ERR_WORKSPACE;
   mla_status st = check_shape(B, H, Tq, Tk, past_len);
@@ -198,6 +219,7 @@ mla_status attention_impl(const uint16_t* q_nope, const uint16_t* q_pe, const ui
     const int chunk = pl.chunk, splits = pl.splits;
     if (splits > 65535) return MLA_ERR_ARG;
     if (workspace_bytes < decode_workspace(B, H, splits)) return MLA_ERR_WORKSPACE;
+    if (check_only) return MLA_OK;
     DecodeArgs a{};
     a.q_nope = q_nope; a.q_pe = q_pe; a.k_nope = k_nope; a.k_pe = k_pe_shared; a.v = v;
     a.kv_len = kv_len; a.out = out; a.status = status;
@@ -216,6 +238,7 @@ mla_status attention_impl(const uint16_t* q_nope, const uint16_t* q_pe, const ui
   }
 
   if (workspace_bytes < kStatusBytes) return MLA_ERR_WORKSPACE;
+  if (check_only) return MLA_OK;
   PrefillArgs a{};
   a.q_nope = q_nope; a.q_pe = q_pe; a.k_nope = k_nope; a.k_pe = k_pe_shared; a.v = v;
   a.kv_len = kv_len; a.out = out; a.status = status;
@@ -264,18 +287,9 @@ mla_status mla_attn_append_fwd(const uint16_t* q_nope, const uint16_t* q_pe,
   }
   // Prefill: the checks run first (nothing is enqueued on failure), then the copy kernel
   // appends the new rows, then attention reads the cache.
-  if (!q_nope || !q_pe || !out) return MLA_ERR_NULL;
-  mla_status st = check_shape(B, H, Tq, Tk, past_len);
-  if (st != MLA_OK) return st;
-  if (!workspace) return MLA_ERR_WORKSPACE;
-  if (workspace_bytes < kStatusBytes) return MLA_ERR_WORKSPACE;
-  if (!aligned16(k_nope_cache) || !aligned16(k_pe_cache) || !aligned16(v_cache) ||
-      !aligned16(q_nope) || !aligned16(q_pe) || !aligned16(out) || !aligned16(workspace) ||
-      (reinterpret_cast<uintptr_t>(kv_len) & 3u) != 0)
-    return MLA_ERR_ALIGN;
-  if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.0f)) return MLA_ERR_ARG;
-  if ((int64_t)B * H * T_cap * 128 > kMaxElems) return MLA_ERR_SHAPE;
-  st = check_device(nullptr);
+  mla_status st = attention_impl(q_nope, q_pe, k_nope_cache, k_pe_cache, v_cache, kv_len, B, H,
+                                 Tq, Tk, past_len, softmax_scale, out, workspace,
+                                 workspace_bytes, cuda_stream, nullptr, T_cap, nullptr, true);
   if (st != MLA_OK) return st;
   AppendArgs ap;
   ap.new_k_nope = k_nope_new; ap.new_k_pe = k_pe_new; ap.new_v = v_new;
@@ -286,6 +300,90 @@ mla_status mla_attn_append_fwd(const uint16_t* q_nope, const uint16_t* q_pe,
   return attention_impl(q_nope, q_pe, k_nope_cache, k_pe_cache, v_cache, kv_len, B, H, Tq, Tk,
                         past_len, softmax_scale, out, workspace, workspace_bytes, cuda_stream,
                         nullptr, T_cap, nullptr);
+}
+
+mla_status mla_rope_frequencies(const mla_rope_config* cfg, double* inv_freq,
+                                double* mscale_ratio) {
+  if (!cfg) return MLA_ERR_NULL;
+  if (!rope_config_ok(*cfg)) return MLA_ERR_ARG;
+  double f[32], m = 1.0;
+  yarn_frequencies(*cfg, f, &m);
+  if (inv_freq) std::memcpy(inv_freq, f, sizeof(f));
+  if (mscale_ratio) *mscale_ratio = m;
+  return MLA_OK;
+}
+
+mla_status mla_rope_table(const mla_rope_config* cfg, int max_pos, float* table,
+                          void* cuda_stream) {
+  if (!cfg || !table) return MLA_ERR_NULL;
+  if (max_pos < 1) return MLA_ERR_SHAPE;
+  if (!aligned16(table)) return MLA_ERR_ALIGN;
+  if (!rope_config_ok(*cfg)) return MLA_ERR_ARG;
+  const mla_status st = check_device(nullptr);
+  if (st != MLA_OK) return st;
+  return launch_rope_table(table, max_pos, *cfg, static_cast<cudaStream_t>(cuda_stream)) ==
+                 cudaSuccess
+             ? MLA_OK
+             : MLA_ERR_CUDA;
+}
+
+size_t mla_attn_rope_workspace_bytes(int B, int H, int Tq, int Tk) {
+  const size_t base = mla_attn_workspace_bytes(B, H, Tq, Tk);
+  if (base == 0) return 0;
+  return round256(base) + rope_bytes(B, H, Tq);
+}
+
+mla_status mla_attn_rope_append_fwd(const uint16_t* q_nope, const uint16_t* q_pe_raw,
+                                    const uint16_t* k_nope_new, const uint16_t* k_pe_new_raw,
+                                    const uint16_t* v_new, uint16_t* k_nope_cache,
+                                    uint16_t* k_pe_cache, uint16_t* v_cache,
+                                    const int32_t* kv_len, int B, int H, int Tq, int T_cap,
+                                    int past_len, float softmax_scale, const float* rope_table,
+                                    int table_rows, uint16_t* out, void* workspace,
+                                    size_t workspace_bytes, void* cuda_stream) {
+  if (!q_pe_raw || !k_nope_new || !k_pe_new_raw || !v_new || !k_nope_cache || !k_pe_cache ||
+      !v_cache || !rope_table)
+    return MLA_ERR_NULL;
+  if (B < 1 || H < 1 || Tq < 1 || past_len < 0 || (int64_t)past_len + Tq > (int64_t)T_cap)
+    return MLA_ERR_SHAPE;
+  const int Tk = past_len + Tq;
+  if (table_rows < Tk) return MLA_ERR_SHAPE;
+  if (!aligned16(q_pe_raw) || !aligned16(k_nope_new) || !aligned16(k_pe_new_raw) ||
+      !aligned16(v_new) || !aligned16(rope_table))
+    return MLA_ERR_ALIGN;
+  if (!workspace) return MLA_ERR_WORKSPACE;
+  const size_t base = mla_attn_workspace_bytes(B, H, Tq, Tk);
+  if (base == 0) return MLA_ERR_SHAPE;
+  if (workspace_bytes < round256(base) + rope_bytes(B, H, Tq)) return MLA_ERR_WORKSPACE;
+  uint8_t* rot = static_cast<uint8_t*>(workspace) + round256(base);
+  uint16_t* q_pe_rot = reinterpret_cast<uint16_t*>(rot);
+  uint16_t* k_pe_rot = reinterpret_cast<uint16_t*>(rot + q_rot_bytes(B, H, Tq));
+
+  // Every check of the attention call runs before anything is enqueued.
+  AppendPtrs app = {k_nope_new, k_pe_rot, v_new, k_nope_cache, k_pe_cache, v_cache};
+  const AppendPtrs* fused = Tq == 1 ? &app : nullptr;
+  mla_status st = attention_impl(q_nope, q_pe_rot, k_nope_cache, k_pe_cache, v_cache, kv_len, B,
+                                 H, Tq, Tk, past_len, softmax_scale, out, workspace,
+                                 workspace_bytes, cuda_stream, nullptr, T_cap, fused, true);
+  if (st != MLA_OK) return st;
+
+  RopeAppendArgs r{};
+  r.q_pe_raw = q_pe_raw; r.q_pe_rot = q_pe_rot; r.k_pe_raw = k_pe_new_raw;
+  r.cos_sin = rope_table;
+  r.B = B; r.H = H; r.Tq = Tq; r.past_len = past_len; r.kv_rows = T_cap;
+  if (Tq == 1) {
+    // Decode: rotate into the workspace; the decode kernel appends all three new rows.
+    r.k_pe_dst = k_pe_rot; r.k_pe_rows = 1; r.k_pe_row0 = 0;
+  } else {
+    r.k_pe_dst = k_pe_cache; r.k_pe_rows = T_cap; r.k_pe_row0 = past_len;
+    r.new_k_nope = k_nope_new; r.new_v = v_new;
+    r.cache_k_nope = k_nope_cache; r.cache_v = v_cache;
+  }
+  if (launch_rope_append(r, static_cast<cudaStream_t>(cuda_stream)) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return attention_impl(q_nope, q_pe_rot, k_nope_cache, k_pe_cache, v_cache, kv_len, B, H, Tq,
+                        Tk, past_len, softmax_scale, out, workspace, workspace_bytes,
+                        cuda_stream, nullptr, T_cap, fused);
 }
 
 mla_status mla_attn_fwd(const uint16_t* q_nope, const uint16_t* q_pe, const uint16_t* k_nope,

@@ -4,6 +4,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "mla_attn.h"
+
 namespace mla {
 
 // Decode (Tq == 1): split-KV partial pass, then a combine pass when there are several
@@ -82,6 +84,32 @@ struct AppendArgs {
   int B, H, Tq, past_len, kv_rows;
 };
 cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream);
+
+// YaRN frequencies and mscale ratio of a configuration (host arithmetic, double).
+void yarn_frequencies(const mla_rope_config& cfg, double* inv_freq, double* mscale);
+
+// cos / sin table [max_pos][64] (cos in columns 0..31, sin in 32..63, times the ratio).
+cudaError_t launch_rope_table(float* cos_sin, int max_pos, const mla_rope_config& cfg,
+                              cudaStream_t stream);
+
+// Rotary pre-pass: query t and new rotary key t are rotated at position past_len + t.
+// Rotated queries go to q_pe_rot [B,H,Tq,64]; rotated keys (b, t) to
+// k_pe_dst + ((b * k_pe_rows) + k_pe_row0 + t) * 64.  When new_k_nope is non-null the
+// no-rope key and value rows are also appended to the caches at rows past_len + t.
+struct RopeAppendArgs {
+  const uint16_t* q_pe_raw;
+  uint16_t* q_pe_rot;
+  const uint16_t* k_pe_raw;
+  uint16_t* k_pe_dst;
+  int k_pe_rows, k_pe_row0;
+  const uint16_t* new_k_nope;
+  const uint16_t* new_v;
+  uint16_t* cache_k_nope;
+  uint16_t* cache_v;
+  const float* cos_sin;
+  int B, H, Tq, past_len, kv_rows;
+};
+cudaError_t launch_rope_append(const RopeAppendArgs& a, cudaStream_t stream);
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();

@@ -328,5 +328,21 @@ void mla_oracle_yarn(double theta, double factor, double orig_max_pos, double be
   *mscale_ratio = m1 / m2;
 }
 
+/*
+ * The rotary step alone: row r of x ([n][64] bf16 bits) rotated at position pos[r] into
+ * out ([n][64] doubles), with the frequencies and mscale ratio of mla_oracle_yarn.  Used to
+ * check rotated rows that a cache holds.
+ */
+int mla_oracle_rotate(const uint16_t* x, const int64_t* pos, int64_t n, const double* inv_freq,
+                      double mscale, double* out) {
+  if (!x || !pos || !inv_freq || !out || n < 0) return 1;
+  for (int64_t r = 0; r < n; ++r) {
+    double raw[D_ROPE];
+    for (int d = 0; d < D_ROPE; ++d) raw[d] = bf16_to_double(x[r * D_ROPE + d]);
+    rotate64(out + r * D_ROPE, raw, (double)pos[r], inv_freq, mscale);
+  }
+  return 0;
+}
+
 /* Exposed for the test that pins the diagnostic rounding against torch's own cast. */
 double mla_oracle_round_bf16(double x) { return round_bf16(x); }

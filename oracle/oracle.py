@@ -67,6 +67,8 @@ def _load():
             d = ctypes.c_double
             lib.mla_oracle_yarn.restype = None
             lib.mla_oracle_yarn.argtypes = [d, d, d, d, d, d, d, p, p]
+            lib.mla_oracle_rotate.restype = ctypes.c_int
+            lib.mla_oracle_rotate.argtypes = [p, p, i64, p, d, p]
             _lib = lib
     return _lib
 
@@ -152,6 +154,25 @@ def yarn(theta: float, factor: float, orig_max_pos: int, beta_fast: float, beta_
                         float(beta_slow), float(mscale), float(mscale_all_dim), f.ctypes.data,
                         r.ctypes.data)
     return f, float(r[0])
+
+
+def rotate(x, positions, inv_freq, mscale: float):
+    """The rotary step alone: rows of x ([..., 64] bf16) rotated at positions (broadcast to
+    x's leading shape, one per row); returns fp64 [..., 64]."""
+    lib = _load()
+    xb = _bits(x)
+    shape = xb.shape
+    assert shape[-1] == 64
+    rows = np.ascontiguousarray(xb.reshape(-1, 64))
+    pos = np.ascontiguousarray(np.broadcast_to(np.asarray(positions, dtype=np.int64),
+                                               shape[:-1]).reshape(-1))
+    out = np.empty((rows.shape[0], 64), dtype=np.float64)
+    f = np.ascontiguousarray(np.asarray(inv_freq, dtype=np.float64).reshape(32))
+    rc = lib.mla_oracle_rotate(rows.ctypes.data, pos.ctypes.data, rows.shape[0], f.ctypes.data,
+                               float(mscale), out.ctypes.data)
+    if rc != 0:
+        raise ValueError(f"oracle rejected its arguments (code {rc})")
+    return out.reshape(shape)
 
 
 def oracle_rows_rope(q_nope, q_pe_raw, k_nope, k_pe, v, kv_len, past_len: int,

@@ -19,7 +19,7 @@ import numpy as np
 import pytest
 import torch
 
-from oracle import oracle_rows, oracle_rows_rope, yarn
+from oracle import oracle_rows, oracle_rows_rope, rotate, yarn
 from mla_causal_attention_gb300.workloads import softmax_scale_192
 
 PAGE = dict(theta=50000.0, factor=32.0, orig_max_pos=4096, beta_fast=1.0, beta_slow=1.0,
@@ -103,3 +103,41 @@ def test_single_frequency_closed_form(dim):
         e = np.array([math.exp(s[j]) for j in vis])
         want = (e[:, None] * v[vis]).sum(0) / e.sum()
         np.testing.assert_allclose(out[i], want, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("dim", [0, 7, 19, 20, 31])
+def test_rotate_unit_vectors(dim):
+    """The rotation alone on unit vectors: e_d at position p goes to cos(p f_d) e_d +
+    sin(p f_d) e_{d+32}, and e_{d+32} to -sin(p f_d) e_d + cos(p f_d) e_{d+32} (a
+    counter-clockwise turn of the pair by the angle p f_d), times the mscale ratio."""
+    f, _ = yarn(**PAGE)
+    x = torch.zeros(2, 64, dtype=torch.bfloat16)
+    x[0, dim] = 1.0
+    x[1, dim + 32] = 1.0
+    for p in (1, 4095, 131071):
+        for ratio in (1.0, 1.25):
+            y = rotate(x, p, f, ratio)
+            a = p * f[dim]
+            want = np.zeros((2, 64))
+            want[0, dim], want[0, dim + 32] = math.cos(a), math.sin(a)
+            want[1, dim], want[1, dim + 32] = -math.sin(a), math.cos(a)
+            np.testing.assert_allclose(y, want * ratio, rtol=0, atol=1e-15)
+
+
+def test_rotate_is_the_step_inside_attention():
+    """Rotating the query and the new keys with rotate() at positions past_len + t, rounding
+    them to bf16 and running the rotation-free oracle matches oracle_rows_rope up to that
+    rounding (about 1e-3 here); a position off by one in either moves the output by 0.1."""
+    past, Tq = 7, 5
+    d = _case(1, 2, Tq, past, seed=5)
+    f, r = yarn(**PAGE)
+    sc = softmax_scale_192()
+    want = oracle_rows_rope(d["q_nope"], d["q_pe"], d["k_nope"], d["k_pe_shared"], d["v"],
+                            None, past, sc, f, r)
+    pos = np.arange(Tq) + past
+    q_rot = torch.from_numpy(rotate(d["q_pe"], pos[None, None, :], f, r)).to(torch.bfloat16)
+    k_rot = d["k_pe_shared"].clone()
+    k_rot[:, past:] = torch.from_numpy(
+        rotate(d["k_pe_shared"][:, past:], pos[None, :], f, r)).to(torch.bfloat16)
+    got = oracle_rows(d["q_nope"], q_rot, d["k_nope"], k_rot, d["v"], None, past, sc)
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-2)
