@@ -7,9 +7,13 @@
 // softmax, bf16 weights, weighted sum of values), evaluated flash-style so the [Tq, Tk]
 // score matrix never leaves the SM.
 //
-// Work unit (one CTA): one (b, h) and a pair of 128-row query tiles (256 rows).
+// Work unit: one (b, h) and a pair of 128-row query tiles (256 rows).  The kernel is
+// persistent: one CTA per SM walks its units (heaviest first, snake order across CTAs)
+// with TMEM allocated and barriers initialised once, so a unit's query load and the
+// previous unit's output stores overlap the tensor-core work of their neighbours.
 // Warp roles (384 threads):
-//   warp 0      TMA producer: both query tiles once, then for every 128-key tile five
+//   warp 0      TMA producer: per unit both query tiles (each as soon as the previous
+//               unit's last score MMA on it has run), then for every 128-key tile five
 //               16 KB sub-tiles (k_nope cols 0-63, k_nope cols 64-127, the shared
 //               rotary key, v cols 0-63, v cols 64-127) into an 8-slot ring.
 //   warp 1      allocates all 512 TMEM columns; lane 0 issues the MMAs:
@@ -24,8 +28,9 @@
 //               causal/padding mask only on tiles that straddle the limit, keeps a
 //               running max (log2 domain) and sum, writes bf16 P over the S columns, and
 //               rescales its O row only when the max grows by more than 2^8 (the stale
-//               max cancels exactly in O / l).  At the end it normalises O and stores
-//               the bf16 row.
+//               max cancels exactly in O / l).  At the end of a unit it moves O to
+//               registers, releases the O columns for the next unit's first value mix,
+//               then normalises and stores the bf16 row.
 // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512).
 #include <cuda.h>
 
@@ -65,28 +70,35 @@ struct PrefillParams {
   float scale_log2;
 };
 
-// K/V tiles are tracked as groups (one K tile = 3 sub-tiles, one V tile = 2), double-
-// buffered by key-tile parity: at most two tiles of each kind are in flight.
+// Barriers.  K/V tiles are counted over the CTA's whole run (g = 0, 1, ...) and
+// double-buffered by tile parity; score steps are counted per query tile over the run;
+// Q, O-done and O-free advance once per work unit.
 struct Bars {
-  uint64_t kfull[2];   // K(j) landed (3 TMA boxes, one transaction count)
-  uint64_t vfull[2];   // V(j) landed (2 boxes)
-  uint64_t kempty[2];  // K(j) slots released (MMA commit after both score MMAs)
-  uint64_t vempty[2];  // V(j) slots released (MMA commit after both value mixes)
-  uint64_t q_full;
-  uint64_t s_full[2];
-  uint64_t p_ready[2];  // P_t written to TMEM (4 warp arrivals)
-  uint64_t o_done[2];
+  uint64_t kfull[2];    // K(g) landed (3 TMA boxes, one transaction count)
+  uint64_t vfull[2];    // V(g) landed (2 boxes)
+  uint64_t kempty[2];   // K(g) slots released (MMA commit after both score MMAs)
+  uint64_t vempty[2];   // V(g) slots released (MMA commit after both value mixes)
+  uint64_t q_full[2];   // Q_t of the unit landed
+  uint64_t q_empty[2];  // last score MMA of tile t of the unit done: Q_t may be refilled
+  uint64_t s_full[2];   // S_t of a step in TMEM
+  uint64_t p_ready[2];  // P_t of a step in TMEM (4 warp arrivals)
+  uint64_t o_done[2];   // last value mix of tile t of the unit done
+  uint64_t o_free[2];   // O_t of the unit read out by the softmax warps (4 warp arrivals)
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort_flag;
 };
 static_assert(sizeof(Bars) <= 256, "barrier block");
 
-__device__ __forceinline__ void setmaxnreg_dec56() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
+// Register split of the 384 x 168 registers the block launches with: 88 for the
+// producer / MMA warpgroup, 208 for the two softmax warpgroups (128 x 88 + 256 x 208 =
+// 64512, the whole pool).
+static_assert(128 * 88 + 256 * 208 <= kThreads * 168, "register split");
+__device__ __forceinline__ void setmaxnreg_dec_control() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 88;" ::: "memory");
 }
-__device__ __forceinline__ void setmaxnreg_inc224() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 224;" ::: "memory");
+__device__ __forceinline__ void setmaxnreg_inc_softmax() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 208;" ::: "memory");
 }
 
 // Keeps the compiler from using tcgen05.ld destinations before tcgen05.wait::ld.
@@ -114,6 +126,55 @@ __device__ __forceinline__ void tma_load_3d_nohint(void* smem_dst, const void* t
       : "memory");
 }
 
+// One work unit: a pair of 128-row query tiles of one (b, h).  Units are numbered
+// heaviest first (the last query tiles see the most keys); CTA c of G takes units
+// i G + c in even rounds i and i G + (G - 1 - c) in odd ones, which balances the
+// decreasing sizes as well as dynamic assignment would, with no shared counter.
+struct Unit {
+  int bh, b, r0, kvl, nt0, nt1, n;
+  __device__ __forceinline__ int nt(int t) const { return t ? nt1 : nt0; }
+};
+
+// Unit index of the CTA's i-th unit, or -1 past the end.
+__device__ __forceinline__ int unit_index(const PrefillParams& p, int i) {
+  const int G = gridDim.x;
+  const int64_t k = (int64_t)i * G + ((i & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
+  return k < (int64_t)p.B * p.H * p.n_qb ? (int)k : -1;
+}
+
+// kv_len of a unit's sequence as stored (unclamped), or Tk without kv_len.  The only
+// global load of a unit's description: each role fetches it one unit ahead.
+__device__ __forceinline__ int unit_kv(const PrefillParams& p, int unit) {
+  if (unit < 0 || !p.kv_len) return p.Tk;
+  return p.kv_len[(unit % (p.B * p.H)) / p.H];
+}
+
+__device__ __forceinline__ Unit unit_make(const PrefillParams& p, int unit, int kv) {
+  Unit w;
+  const int BH = p.B * p.H;
+  const int qb = p.n_qb - 1 - unit / BH;
+  w.bh = unit % BH;
+  w.b = w.bh / p.H;
+  w.r0 = qb * 2 * kBM;
+  w.kvl = min(max(kv, 1), p.Tk);
+  int nt[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int rt = w.r0 + t * kBM;
+    if (rt >= p.Tq) {
+      nt[t] = 0;
+    } else {
+      const int qlast = min(rt + kBM - 1, p.Tq - 1);
+      const int lastkey = min(qlast + p.past_len, w.kvl - 1);
+      nt[t] = lastkey / kBN + 1;
+    }
+  }
+  w.nt0 = nt[0];
+  w.nt1 = nt[1];
+  w.n = max(nt[0], nt[1]);
+  return w;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     mla_prefill_kernel(const __grid_constant__ PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -124,33 +185,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
   volatile int* abort_flag = &bars->abort_flag;
 
-  // ---- work unit: heaviest query-tile pairs first ----
-  const int BH = p.B * p.H;
-  const int unit = blockIdx.x;
-  const int qb = p.n_qb - 1 - unit / BH;
-  const int bh = unit % BH;
-  const int b = bh / p.H;
-  const int r0 = qb * 2 * kBM;
-
-  int kvl = p.kv_len ? p.kv_len[b] : p.Tk;
-  if (kvl < 1 || kvl > p.Tk) {
-    if (threadIdx.x == 0) set_status(p.status, MLA_ERR_KVLEN);
-    kvl = min(max(kvl, 1), p.Tk);
-  }
-  int nt[2];
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const int rt = r0 + t * kBM;
-    if (rt >= p.Tq) {
-      nt[t] = 0;
-    } else {
-      const int qlast = min(rt + kBM - 1, p.Tq - 1);
-      const int lastkey = min(qlast + p.past_len, kvl - 1);
-      nt[t] = lastkey / kBN + 1;
-    }
-  }
-  const int n = max(nt[0], nt[1]);
-
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
@@ -160,16 +194,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->vfull[i], 1);
       mbar_init(&bars->kempty[i], 1);
       mbar_init(&bars->vempty[i], 1);
-    }
-    mbar_init(&bars->q_full, 1);
-    for (int t = 0; t < 2; ++t) {
-      mbar_init(&bars->s_full[t], 1);
-      mbar_init(&bars->p_ready[t], 4);
-      mbar_init(&bars->o_done[t], 1);
+      mbar_init(&bars->q_full[i], 1);
+      mbar_init(&bars->q_empty[i], 1);
+      mbar_init(&bars->s_full[i], 1);
+      mbar_init(&bars->p_ready[i], 4);
+      mbar_init(&bars->o_done[i], 1);
+      mbar_init(&bars->o_free[i], 4);
     }
     mbar_init(&bars->mma_done, 1);
     bars->abort_flag = 0;
     fence_barrier_init();
+    // Out-of-range kv_len is reported once per CTA that meets it (and clamped).
+    for (int i = 0;; ++i) {
+      const int u = unit_index(p, i);
+      if (u < 0) break;
+      const int raw = unit_kv(p, u);
+      if (raw < 1 || raw > p.Tk) {
+        set_status(p.status, MLA_ERR_KVLEN);
+        break;
+      }
+    }
   }
   if (warp == 1) {
     tc::tmem_alloc(&bars->tmem_base, 512);
@@ -181,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = bars->tmem_base;
 
   if (warp < 4) {
-    setmaxnreg_dec56();
+    setmaxnreg_dec_control();
     if (warp == 0 && lane == 0) {
       // ================= TMA producer =================
       prefetch_tmap(&p.tm_qn);
@@ -190,15 +234,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&p.tm_kr);
       prefetch_tmap(&p.tm_v);
       const uint64_t pol_q = l2_policy_evict_first();
-      const uint32_t qbytes = (uint32_t)((nt[0] > 0 ? 3 : 0) + (nt[1] > 0 ? 3 : 0)) * kSub;
-      mbar_arrive_expect_tx(&bars->q_full, qbytes);
-      for (int t = 0; t < 2; ++t) {
-        if (nt[t] == 0) continue;
-        const int rt = r0 + t * kBM;
-        tma_load_3d(sQ + (t * 3 + 0) * kSub, &p.tm_qn, &bars->q_full, 0, rt, bh, pol_q);
-        tma_load_3d(sQ + (t * 3 + 1) * kSub, &p.tm_qn, &bars->q_full, 64, rt, bh, pol_q);
-        tma_load_3d(sQ + (t * 3 + 2) * kSub, &p.tm_qr, &bars->q_full, 0, rt, bh, pol_q);
-      }
       // Sub-tile u goes to slot u % kSlots, whose previous occupant was sub-tile
       // u - kSlots of key tile (u - kSlots) / 5; that tile's K or V group must have been
       // released by the MMAs before the slot is overwritten.
@@ -209,49 +244,82 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint64_t* bar = (prev % kSubPerKv) < 3 ? &bars->kempty[st & 1] : &bars->vempty[st & 1];
         return mbar_wait(bar, (st >> 1) & 1, p.status, abort_flag);
       };
-      uint32_t u = 0;
-      bool ok = true;
-      int k_posted = 0, v_posted = 0;  // groups whose transaction count has been posted
-      for (int j = 0; j < n && ok; ++j, u += kSubPerKv) {
-        const int jt = j * kBN;
-        // K(j): no-rope columns 0-63, 64-127 and the shared rotary tile, one barrier.
-        uint64_t* kb = &bars->kfull[j & 1];
-        for (int s = 0; s < 3 && ok; ++s) {
-          ok = slot_free(u + s);
-          if (!ok) break;
-          if (s == 0) {
-            mbar_arrive_expect_tx(kb, 3 * kSub);
-            k_posted = j + 1;
-          }
-          uint8_t* dst = sRing + ((u + s) & (kSlots - 1)) * kSub;
-          if (s < 2)
-            tma_load_3d_nohint(dst, &p.tm_kn, kb, 64 * s, jt, bh);
-          else
-            tma_load_3d_nohint(dst, &p.tm_kr, kb, 0, jt, b);
+      // Q_t of unit i: sQ_t is free once the previous unit's last score MMA on tile t has
+      // run (one q_empty phase per unit).
+      auto load_q = [&](int i, int t, const int r0, const int ntt, const int bh) -> bool {
+        if (i > 0 && !mbar_wait(&bars->q_empty[t], (i - 1) & 1, p.status, abort_flag))
+          return false;
+        if (ntt == 0) {
+          mbar_arrive(&bars->q_full[t]);  // nothing to load: complete the phase
+          return true;
         }
-        if (!ok) break;
-        // V(j): columns 0-63 go to the lower-addressed of its two slots, so one MMA with a
-        // positive leading-byte offset covers all 128 value columns.
-        uint64_t* vb = &bars->vfull[j & 1];
-        const uint32_t sa = (u + 3) & (kSlots - 1), sb = (u + 4) & (kSlots - 1);
-        ok = slot_free(u + 3) && slot_free(u + 4);
-        if (!ok) break;
-        mbar_arrive_expect_tx(vb, 2 * kSub);
-        v_posted = j + 1;
-        tma_load_3d_nohint(sRing + min(sa, sb) * kSub, &p.tm_v, vb, 0, jt, bh);
-        tma_load_3d_nohint(sRing + max(sa, sb) * kSub, &p.tm_v, vb, 64, jt, bh);
+        mbar_arrive_expect_tx(&bars->q_full[t], 3 * kSub);
+        const int rt = r0 + t * kBM;
+        uint8_t* dst = sQ + t * 3 * kSub;
+        tma_load_3d(dst, &p.tm_qn, &bars->q_full[t], 0, rt, bh, pol_q);
+        tma_load_3d(dst + kSub, &p.tm_qn, &bars->q_full[t], 64, rt, bh, pol_q);
+        tma_load_3d(dst + 2 * kSub, &p.tm_qr, &bars->q_full[t], 0, rt, bh, pol_q);
+        return true;
+      };
+      uint32_t u = 0;   // ring sub-tiles issued over the run
+      uint32_t g = 0;   // key tiles issued over the run
+      int q_units = 0;  // units whose Q transactions have been posted
+      bool ok = true;
+      int kv_next = unit_kv(p, unit_index(p, 0));
+      for (int i = 0; ok; ++i) {
+        const int unit = unit_index(p, i);
+        if (unit < 0) break;
+        const Unit w = unit_make(p, unit, kv_next);
+        kv_next = unit_kv(p, unit_index(p, i + 1));  // fetched a unit ahead
+        ok = load_q(i, 0, w.r0, w.nt0, w.bh);
+        q_units = i + 1;
+        for (int j = 0; j < w.n && ok; ++j, ++g, u += kSubPerKv) {
+          const int jt = j * kBN;
+          // K(j): no-rope columns 0-63, 64-127 and the shared rotary tile, one barrier.
+          uint64_t* kb = &bars->kfull[g & 1];
+          for (int s = 0; s < 3 && ok; ++s) {
+            ok = slot_free(u + s);
+            if (!ok) break;
+            if (s == 0) mbar_arrive_expect_tx(kb, 3 * kSub);
+            uint8_t* dst = sRing + ((u + s) & (kSlots - 1)) * kSub;
+            if (s < 2)
+              tma_load_3d_nohint(dst, &p.tm_kn, kb, 64 * s, jt, w.bh);
+            else
+              tma_load_3d_nohint(dst, &p.tm_kr, kb, 0, jt, w.b);
+          }
+          if (!ok) break;
+          // Q of the second tile after the first key tile: the first score MMA needs only
+          // Q_0 and K(0).
+          if (j == 0) {
+            ok = load_q(i, 1, w.r0, w.nt1, w.bh);
+            if (!ok) break;
+          }
+          // V(j): columns 0-63 go to the lower-addressed of its two slots, so one MMA with
+          // a positive leading-byte offset covers all 128 value columns.
+          uint64_t* vb = &bars->vfull[g & 1];
+          const uint32_t sa = (u + 3) & (kSlots - 1), sb = (u + 4) & (kSlots - 1);
+          ok = slot_free(u + 3) && slot_free(u + 4);
+          if (!ok) break;
+          mbar_arrive_expect_tx(vb, 2 * kSub);
+          tma_load_3d_nohint(sRing + min(sa, sb) * kSub, &p.tm_v, vb, 0, jt, w.bh);
+          tma_load_3d_nohint(sRing + max(sa, sb) * kSub, &p.tm_v, vb, 64, jt, w.bh);
+        }
       }
-      // Every load this thread issued must land before shared memory is released.
-      drain_wait(&bars->q_full, 0);
-      for (int j = max(0, k_posted - 2); j < k_posted; ++j)
-        drain_wait(&bars->kfull[j & 1], (j >> 1) & 1);
-      for (int j = max(0, v_posted - 2); j < v_posted; ++j)
-        drain_wait(&bars->vfull[j & 1], (j >> 1) & 1);
+      // Every load this thread issued must land before shared memory is released.  Each
+      // barrier has at most one phase in flight (the next one is posted only after the
+      // consumer released the previous), so waiting for the last posted phases suffices.
+      if (q_units > 0) {
+        drain_wait(&bars->q_full[0], (q_units - 1) & 1);
+        drain_wait(&bars->q_full[1], (q_units - 1) & 1);
+      }
+      for (uint32_t k = (g >= 2 ? g - 2 : 0); k < g; ++k) {
+        drain_wait(&bars->kfull[k & 1], (k >> 1) & 1);
+        drain_wait(&bars->vfull[k & 1], (k >> 1) & 1);
+      }
     } else if (warp == 1) {
       // ================= MMA issuer =================
       // The whole warp runs this loop (waits, descriptor arithmetic: warp-uniform values);
-      // one elected lane issues each batch of MMAs and commits.  Each MMA keeps the tensor
-      // core busy for only 32-64 cycles, so issue must be cheap: descriptors are built once
+      // one elected lane issues each batch of MMAs and commits.  Descriptors are built once
       // (their high word is constant) and per MMA only the start-address field moves.
       constexpr uint32_t kIdescQK = tc::idesc_bf16_f32(128, 128, false);
       constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(128, 128, true);
@@ -264,76 +332,111 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dhi_v_far = tc::smem_desc_sw128(0, (kSlots - 1) * kSub, 1024);
       const uint32_t q_lo = smem_u32(sQ) >> 4;
       const uint32_t ring_lo = smem_u32(sRing) >> 4;
-      bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_full, 0, p.status, abort_flag));
-      tc::fence_after_sync();
-      for (int j = 0; j <= n && ok; ++j) {
-        const uint32_t uk = (uint32_t)j * kSubPerKv;  // sub-tiles of K(j): uk .. uk+2
-        const uint32_t uv = uk - 2u;                   // sub-tiles of V(j-1): uv, uv+1
-        uint32_t klo[3];
+      uint32_t g = 0;             // key tiles consumed over the run
+      uint32_t stp[2] = {0, 0};   // value mixes issued per tile over the run
+      bool ok = true;
+      int kv_next = unit_kv(p, unit_index(p, 0));
+      for (int i = 0; ok; ++i) {
+        const int unit = unit_index(p, i);
+        if (unit < 0) break;
+        const Unit w = unit_make(p, unit, kv_next);
+        kv_next = unit_kv(p, unit_index(p, i + 1));  // fetched a unit ahead
+        for (int j = 0; j <= w.n && ok; ++j) {
+          const uint32_t gk = g + (uint32_t)j;           // key tile j of this unit
+          const uint32_t uk = gk * kSubPerKv;            // its sub-tiles: uk .. uk+2
+          const uint32_t uv = uk - 2u;                   // sub-tiles of V(j-1): uv, uv+1
+          uint32_t klo[3];
 #pragma unroll
-        for (int s = 0; s < 3; ++s) klo[s] = ring_lo + ((uk + s) & (kSlots - 1)) * kSubLo;
-        const uint32_t va = uv & (kSlots - 1), vb2 = (uv + 1) & (kSlots - 1);
-        const uint32_t vlo = ring_lo + min(va, vb2) * kSubLo;
-        const uint64_t dhi_v = vb2 > va ? dhi_v_near : dhi_v_far;
-        // V(j-1) first: the value mix of tile 0 can start while K(j) is still landing.
-        if (j > 0) ok = mbar_wait(&bars->vfull[(j - 1) & 1], ((j - 1) >> 1) & 1, p.status, abort_flag);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        tc::fence_after_sync();
-        bool k_landed = false;
-#pragma unroll 1
-        for (int t = 0; t < 2; ++t) {
-          const uint32_t s_tmem = tbase + t * 128;
-          const uint32_t o_tmem = tbase + 256 + t * 128;
-          if (j > 0 && j - 1 < nt[t]) {
-            // O_t += P_t(j-1) V(j-1): P from TMEM (aliasing S_t), V MN-major from smem.
-            ok = __all_sync(0xffffffffu,
-                            mbar_wait(&bars->p_ready[t], (j - 1) & 1, p.status, abort_flag));
-            if (!ok) break;
-            tc::fence_after_sync();
-            const uint32_t acc0 = (j > 1) ? 1u : 0u;
-            if (tc::elect_one()) {
+          for (int s = 0; s < 3; ++s) klo[s] = ring_lo + ((uk + s) & (kSlots - 1)) * kSubLo;
+          const uint32_t va = uv & (kSlots - 1), vb2 = (uv + 1) & (kSlots - 1);
+          const uint32_t vlo = ring_lo + min(va, vb2) * kSubLo;
+          const uint64_t dhi_v = vb2 > va ? dhi_v_near : dhi_v_far;
+          // V(j-1) first: the value mix of tile 0 can start while K(j) is still landing.
+          if (j > 0)
+            ok = mbar_wait(&bars->vfull[(gk - 1) & 1], ((gk - 1) >> 1) & 1, p.status,
+                           abort_flag);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          tc::fence_after_sync();
+          bool k_landed = false;
 #pragma unroll
-              for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t bdesc = dhi_v | (uint64_t)(vlo + kk * (2048 >> 4));
-                tc::mma_ts(o_tmem, s_tmem + kk * 8, bdesc, kIdescPV, kk > 0 ? 1u : acc0);
-              }
-              if (j - 1 == nt[t] - 1) tc::commit(&bars->o_done[t]);
-            }
-            __syncwarp();
-          }
-          if (t == 1 && j > 0) {
-            // V(j-1) is no longer needed once both value mixes have run.
-            if (tc::elect_one()) tc::commit(&bars->vempty[(j - 1) & 1]);
-            __syncwarp();
-          }
-          if (j < nt[t]) {
-            if (!k_landed) {
-              ok = __all_sync(0xffffffffu,
-                              mbar_wait(&bars->kfull[j & 1], (j >> 1) & 1, p.status, abort_flag));
+          for (int t = 0; t < 2; ++t) {
+            const uint32_t s_tmem = tbase + t * 128;
+            const uint32_t o_tmem = tbase + 256 + t * 128;
+            if (j > 0 && j - 1 < w.nt(t)) {
+              // O_t += P_t(j-1) V(j-1): P from TMEM (aliasing S_t), V MN-major from smem.
+              ok = mbar_wait(&bars->p_ready[t], stp[t] & 1, p.status, abort_flag);
+              // The unit's first value mix overwrites O_t: the previous unit's O_t must
+              // have been read out.
+              if (ok && j == 1 && i > 0)
+                ok = mbar_wait(&bars->o_free[t], (i - 1) & 1, p.status, abort_flag);
+              ok = __all_sync(0xffffffffu, ok);
               if (!ok) break;
               tc::fence_after_sync();
-              k_landed = true;
-            }
-            // S_t = Q_t K(j)^T over 192 columns: 4 k-steps per 64-column sub-tile.
-            const uint32_t qlo = q_lo + t * 3 * kSubLo;
-            if (tc::elect_one()) {
+              const uint32_t acc0 = (j > 1) ? 1u : 0u;
+              if (tc::elect_one()) {
 #pragma unroll
-              for (int kk = 0; kk < 12; ++kk) {
-                const uint32_t koff = (kk & 3) * (32 >> 4);
-                const uint64_t adesc = dhi_k | (uint64_t)(qlo + (kk >> 2) * kSubLo + koff);
-                const uint64_t bdesc = dhi_k | (uint64_t)(klo[kk >> 2] + koff);
-                tc::mma_ss(s_tmem, adesc, bdesc, kIdescQK, kk > 0 ? 1u : 0u);
+                for (int kk = 0; kk < 8; ++kk) {
+                  const uint64_t bdesc = dhi_v | (uint64_t)(vlo + kk * (2048 >> 4));
+                  tc::mma_ts(o_tmem, s_tmem + kk * 8, bdesc, kIdescPV, kk > 0 ? 1u : acc0);
+                }
+                if (j - 1 == w.nt(t) - 1) tc::commit(&bars->o_done[t]);
               }
-              tc::commit(&bars->s_full[t]);
+              __syncwarp();
+              ++stp[t];
             }
+            if (t == 1 && j > 0) {
+              // V(j-1) is no longer needed once both value mixes have run.
+              if (tc::elect_one()) tc::commit(&bars->vempty[(gk - 1) & 1]);
+              __syncwarp();
+            }
+            if (j < w.nt(t)) {
+              if (j == 0) {
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(&bars->q_full[t], i & 1, p.status, abort_flag));
+                if (!ok) break;
+              }
+              if (!k_landed) {
+                ok = __all_sync(0xffffffffu, mbar_wait(&bars->kfull[gk & 1], (gk >> 1) & 1,
+                                                       p.status, abort_flag));
+                if (!ok) break;
+                k_landed = true;
+              }
+              tc::fence_after_sync();
+              // S_t = Q_t K(j)^T over 192 columns: 4 k-steps per 64-column sub-tile.
+              const uint32_t qlo = q_lo + t * 3 * kSubLo;
+              if (tc::elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < 12; ++kk) {
+                  const uint32_t koff = (kk & 3) * (32 >> 4);
+                  const uint64_t adesc = dhi_k | (uint64_t)(qlo + (kk >> 2) * kSubLo + koff);
+                  const uint64_t bdesc = dhi_k | (uint64_t)(klo[kk >> 2] + koff);
+                  tc::mma_ss(s_tmem, adesc, bdesc, kIdescQK, kk > 0 ? 1u : 0u);
+                }
+                tc::commit(&bars->s_full[t]);
+                if (j == w.nt(t) - 1) tc::commit(&bars->q_empty[t]);
+              }
+              __syncwarp();
+            }
+          }
+          if (!ok) break;
+          if (j < w.n) {
+            if (tc::elect_one()) tc::commit(&bars->kempty[gk & 1]);
             __syncwarp();
           }
         }
-        if (j < n && ok) {
-          if (tc::elect_one()) tc::commit(&bars->kempty[j & 1]);
+        if (!ok) break;
+        // A tile with no rows in this unit still completes its per-unit phases.
+        if (w.nt1 == 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_full[1], i & 1, p.status, abort_flag));
+          if (!ok) break;
+          if (tc::elect_one()) {
+            tc::commit(&bars->q_empty[1]);
+            tc::commit(&bars->o_done[1]);
+          }
           __syncwarp();
         }
+        g += (uint32_t)w.n;
       }
       // No MMA may still be running when TMEM is released.
       if (tc::elect_one()) tc::commit(&bars->mma_done);
@@ -343,131 +446,164 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ================= softmax warpgroups =================
-    setmaxnreg_inc224();
+    setmaxnreg_inc_softmax();
     const int t = (warp >> 2) - 1;  // query tile 0 or 1
     const int tw = threadIdx.x - 128 * (t + 1);
-    const int qi = r0 + t * kBM + tw;  // query row within the sequence
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t s_tmem = tbase + lane_off + t * 128;
     const uint32_t o_tmem = tbase + lane_off + 256 + t * 128;
-    const int limit = min(qi + p.past_len + 1, kvl);  // keys [0, limit) are visible
     const float sl2 = p.scale_log2;
-    float m = -INFINITY;
-    float l = 0.f;
+    uint32_t st = 0;  // score steps of this tile over the run
     bool ok = true;
-    for (int j = 0; j < nt[t]; ++j) {
-      if (!mbar_wait(&bars->s_full[t], j & 1, p.status, abort_flag)) {
-        ok = false;
-        break;
-      }
-      tc::fence_after_sync();
-      uint32_t r[4][32];
+    int kv_next = unit_kv(p, unit_index(p, 0));
+    for (int i = 0; ok; ++i) {
+      const int unit = unit_index(p, i);
+      if (unit < 0) break;
+      const Unit w = unit_make(p, unit, kv_next);
+      kv_next = unit_kv(p, unit_index(p, i + 1));  // fetched a unit ahead
+      const int ntt = w.nt(t);
+      const int qi = w.r0 + t * kBM + tw;  // query row within the sequence
+      const int limit = min(qi + p.past_len + 1, w.kvl);  // keys [0, limit) are visible
+      float m = -INFINITY;
+      float l = 0.f;
+      for (int j = 0; j < ntt; ++j, ++st) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], st & 1, p.status, abort_flag));
+        if (!ok) break;
+        tc::fence_after_sync();
+        uint32_t r[4][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tc::tmem_ld32(s_tmem + c * 32, r[c]);
-      tc::tmem_wait_ld();
+        for (int c = 0; c < 4; ++c) tc::tmem_ld32(s_tmem + c * 32, r[c]);
+        tc::tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) pin32(r[c]);
+        for (int c = 0; c < 4; ++c) pin32(r[c]);
 
-      const int jt = j * kBN;
-      if (jt + kBN > limit) {
+        const int jt = j * kBN;
+        if (jt + kBN > limit) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (jt + c * 32 + e >= limit) r[c][e] = __float_as_uint(-INFINITY);
+        }
+        // Row max: 8 independent chains of three-input maxima (64 instructions for 128
+        // scores; a single 128-long chain would be latency-bound).
+        float mxp[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mxp[k] = -INFINITY;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            if (jt + c * 32 + e >= limit) r[c][e] = __float_as_uint(-INFINITY);
-      }
-      // Row max: 8 independent chains of three-input maxima (64 instructions for 128
-      // scores; a single 128-long chain would be latency-bound).
-      float mxp[8];
+          for (int e = 0; e < 32; e += 2)
+            mxp[(e >> 1) & 7] = fmax3(mxp[(e >> 1) & 7], __uint_as_float(r[c][e]),
+                                      __uint_as_float(r[c][e + 1]));
+        const float mx = fmax3(fmax3(mxp[0], mxp[1], mxp[2]), fmax3(mxp[3], mxp[4], mxp[5]),
+                               fmaxf(mxp[6], mxp[7]));
+        const float m_tile = mx * sl2;
+        if (j == 0) {
+          m = m_tile;
+        } else {
+          const bool need = m_tile > m + kRescaleThreshold;
+          if (__any_sync(0xffffffffu, need)) {
+            const float alpha = need ? ex2_approx(m - m_tile) : 1.0f;
+            if (need) {
+              m = m_tile;
+              l *= alpha;
+            }
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mxp[k] = -INFINITY;
+            for (int c = 0; c < 4; ++c) {
+              uint32_t o[32];
+              tc::tmem_ld32(o_tmem + c * 32, o);
+              tc::tmem_wait_ld();
+              pin32(o);
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int e = 0; e < 32; e += 2)
-          mxp[(e >> 1) & 7] = fmax3(mxp[(e >> 1) & 7], __uint_as_float(r[c][e]),
-                                    __uint_as_float(r[c][e + 1]));
-      const float mx = fmax3(fmax3(mxp[0], mxp[1], mxp[2]), fmax3(mxp[3], mxp[4], mxp[5]),
-                             fmaxf(mxp[6], mxp[7]));
-      const float m_tile = mx * sl2;
-      if (j == 0) {
-        m = m_tile;
-      } else {
-        const bool need = m_tile > m + kRescaleThreshold;
-        if (__any_sync(0xffffffffu, need)) {
-          const float alpha = need ? ex2_approx(m - m_tile) : 1.0f;
-          if (need) {
-            m = m_tile;
-            l *= alpha;
-          }
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t o[32];
-            tc::tmem_ld32(o_tmem + c * 32, o);
-            tc::tmem_wait_ld();
-            pin32(o);
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tc::tmem_st32(o_tmem + c * 32, o);
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              tc::tmem_st32(o_tmem + c * 32, o);
+            }
           }
         }
-      }
-      // p = 2^(s * scale * log2(e) - m): the scale-and-subtract and the row sum run on
-      // fp32 pairs (one instruction per two scores), the exponentials on the MUFU.
-      const uint64_t sl2_2 = f2_pack(sl2, sl2);
-      const uint64_t negm_2 = f2_pack(-m, -m);
-      uint64_t sp2[4] = {0ull, 0ull, 0ull, 0ull};
-      uint32_t pk[2][32];
+        // p = 2^(s * scale * log2(e) - m): the scale-and-subtract and the row sum run on
+        // fp32 pairs (one instruction per two scores), the exponentials on the MUFU.
+        const uint64_t sl2_2 = f2_pack(sl2, sl2);
+        const uint64_t negm_2 = f2_pack(-m, -m);
+        uint64_t sp2[4] = {0ull, 0ull, 0ull, 0ull};
+        uint32_t pk[2][32];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 4; ++c) {
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const uint64_t xv = ffma2(
-              f2_pack(__uint_as_float(r[c][e]), __uint_as_float(r[c][e + 1])), sl2_2, negm_2);
-          float x0, x1;
-          f2_unpack(xv, x0, x1);
-          x0 = ex2_approx(x0);
-          x1 = ex2_approx(x1);
-          sp2[(e >> 1) & 3] = fadd2(sp2[(e >> 1) & 3], f2_pack(x0, x1));
-          pk[c >> 1][(c & 1) * 16 + (e >> 1)] = pack_bf16x2(x0, x1);
+          for (int e = 0; e < 32; e += 2) {
+            const uint64_t xv = ffma2(
+                f2_pack(__uint_as_float(r[c][e]), __uint_as_float(r[c][e + 1])), sl2_2, negm_2);
+            float x0, x1;
+            f2_unpack(xv, x0, x1);
+            x0 = ex2_approx(x0);
+            x1 = ex2_approx(x1);
+            sp2[(e >> 1) & 3] = fadd2(sp2[(e >> 1) & 3], f2_pack(x0, x1));
+            pk[c >> 1][(c & 1) * 16 + (e >> 1)] = pack_bf16x2(x0, x1);
+          }
         }
+        float sa, sb;
+        f2_unpack(fadd2(fadd2(sp2[0], sp2[1]), fadd2(sp2[2], sp2[3])), sa, sb);
+        l += sa + sb;
+        tc::tmem_st32(s_tmem, pk[0]);
+        tc::tmem_st32(s_tmem + 32, pk[1]);
+        tc::tmem_wait_st();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->p_ready[t]);
       }
-      float sa, sb;
-      f2_unpack(fadd2(fadd2(sp2[0], sp2[1]), fadd2(sp2[2], sp2[3])), sa, sb);
-      l += sa + sb;
-      tc::tmem_st32(s_tmem, pk[0]);
-      tc::tmem_st32(s_tmem + 32, pk[1]);
-      tc::tmem_wait_st();
+      if (!ok) break;
+      // The unit's output: wait for the last value mix, move O_t to registers, release
+      // O_t for the next unit, then normalise and store.
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_done[t], i & 1, p.status, abort_flag));
+      if (!ok) break;
+      tc::fence_after_sync();
+      if (ntt == 0) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->o_free[t]);
+        continue;
+      }
+      uint32_t o[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tc::tmem_ld32(o_tmem + c * 32, o[c]);
+      tc::tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) pin32(o[c]);
       tc::fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_ready[t]);
-    }
-    if (ok && nt[t] > 0) {
-      if (mbar_wait(&bars->o_done[t], 0, p.status, abort_flag)) {
-        tc::fence_after_sync();
-        uint32_t o[4][32];
+      if (lane == 0) mbar_arrive(&bars->o_free[t]);
+      const float inv = 1.0f / l;
+      if (qi < p.Tq) {
+        uint16_t* row = p.out + ((size_t)w.bh * p.Tq + qi) * 128;
+        auto pk = [&](int c, int e) {
+          return pack_bf16x2(__uint_as_float(o[c][e]) * inv, __uint_as_float(o[c][e + 1]) * inv);
+        };
+        if ((reinterpret_cast<uintptr_t>(p.out) & 31u) == 0) {
+          // 32-byte stores: each fills one whole sector of the row.
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tc::tmem_ld32(o_tmem + c * 32, o[c]);
-        tc::tmem_wait_ld();
+          for (int c = 0; c < 4; ++c) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) pin32(o[c]);
-        const float inv = 1.0f / l;
-        if (qi < p.Tq) {
-          uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)bh * p.Tq + qi) * 128);
+            for (int v = 0; v < 2; ++v) {
+              const int e = v * 16;
+              asm volatile(
+                  "st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(
+                      row + c * 32 + e),
+                  "r"(pk(c, e)), "r"(pk(c, e + 2)), "r"(pk(c, e + 4)), "r"(pk(c, e + 6)),
+                  "r"(pk(c, e + 8)), "r"(pk(c, e + 10)), "r"(pk(c, e + 12)), "r"(pk(c, e + 14))
+                  : "memory");
+            }
+          }
+        } else {
+          uint4* dst = reinterpret_cast<uint4*>(row);
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
-              uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(o[c][v * 8 + 0]) * inv,
-                                __uint_as_float(o[c][v * 8 + 1]) * inv);
-              w.y = pack_bf16x2(__uint_as_float(o[c][v * 8 + 2]) * inv,
-                                __uint_as_float(o[c][v * 8 + 3]) * inv);
-              w.z = pack_bf16x2(__uint_as_float(o[c][v * 8 + 4]) * inv,
-                                __uint_as_float(o[c][v * 8 + 5]) * inv);
-              w.w = pack_bf16x2(__uint_as_float(o[c][v * 8 + 6]) * inv,
-                                __uint_as_float(o[c][v * 8 + 7]) * inv);
-              dst[c * 4 + v] = w;
+              uint4 q;
+              q.x = pk(c, v * 8 + 0);
+              q.y = pk(c, v * 8 + 2);
+              q.z = pk(c, v * 8 + 4);
+              q.w = pk(c, v * 8 + 6);
+              dst[c * 4 + v] = q;
             }
           }
         }
@@ -641,7 +777,10 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_device = dev;
   }
-  mla_prefill_kernel<<<(unsigned)units, kThreads, kSmemBytes, stream>>>(p);
+  // Persistent: one CTA per SM (at most one per unit), each walking its units.
+  const int sms = device_sm_count();
+  const uint64_t grid = std::min<uint64_t>(units, (uint64_t)(sms > 0 ? sms : 152));
+  mla_prefill_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -60,6 +60,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait that may park the thread until the phase completes (at most the hint, 1 ms).  A
+// parked waiter issues nothing, so it does not take issue slots from the warps that share
+// its scheduler (a spinning waiter measurably slowed the softmax warps next to it).
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(1000000u)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits until the phase with the given parity has completed.  Bounded: after
 // kWaitLimitNs it records MLA_ERR_TIMEOUT, sets *abort and returns false.  Once *abort is
 // set (by this or another thread of the CTA, via shared memory) every later wait returns
@@ -69,15 +84,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 0;; ++it) {
-    if (mbar_try_wait(a, parity)) return true;
-    if ((it & 63u) == 63u) {
-      if (*abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
-        set_status(status, MLA_ERR_TIMEOUT);
-        *abort = 1;
-        return false;
-      }
+  for (;;) {
+    if (mbar_try_wait_hint(a, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      set_status(status, MLA_ERR_TIMEOUT);
+      *abort = 1;
+      return false;
     }
   }
 }
