@@ -82,6 +82,7 @@ static const double MASK_MIN_BF16 = -3.3895313892515355e38;
 typedef struct {
   const uint16_t *q_nope, *q_pe, *k_nope, *k_pe, *v;
   const int32_t* kv_len;
+  const uint8_t* key_mask; /* [B][Tk], 0 = key hidden; NULL = no 2D padding mask */
   int64_t B, H, Tq, Tk, past_len;
   double scale;
   const int64_t* rows;
@@ -155,8 +156,10 @@ static int one_row(const job_t* J, int64_t flat, double* s, double* o, double* w
     if (eager) acc = round_bf16(acc);
     double sj = acc * scale_used;
     if (eager) sj = round_bf16(sj);
-    /* Step 4: additive mask. */
-    const int visible = (j <= i + J->past_len) && (j < kvl);
+    /* Step 4: additive mask.  A key hidden by the causal mask, by the right padding or by
+     * the 2D padding mask gets the one minimum (the masks are merged, not summed). */
+    const int visible = (j <= i + J->past_len) && (j < kvl) &&
+                        (!J->key_mask || J->key_mask[b * J->Tk + j] != 0);
     sj += visible ? 0.0 : MASK_MIN_BF16;
     if (eager) sj = round_bf16(sj);
     s[j] = sj;
@@ -235,7 +238,8 @@ static int rows_impl(const uint16_t* q_nope, const uint16_t* q_pe, const uint16_
                      const uint16_t* k_pe, const uint16_t* v, const int32_t* kv_len, int64_t B,
                      int64_t H, int64_t Tq, int64_t Tk, int64_t past_len, float softmax_scale,
                      const int64_t* rows, int64_t n_rows, int mode, int nthreads, double* out,
-                     double* wsum, const double* rope_inv_freq, double rope_mscale) {
+                     double* wsum, const double* rope_inv_freq, double rope_mscale,
+                     const uint8_t* key_mask) {
   if (B < 1 || H < 1 || Tq < 1 || Tk < 1 || past_len < 0 || Tk != past_len + Tq) return 10;
   if (!q_nope || !q_pe || !k_nope || !k_pe || !v || !out) return 11;
   if (mode != 0 && mode != 1) return 12;
@@ -249,6 +253,7 @@ static int rows_impl(const uint16_t* q_nope, const uint16_t* q_pe, const uint16_
   memset(&J, 0, sizeof J);
   J.q_nope = q_nope; J.q_pe = q_pe; J.k_nope = k_nope; J.k_pe = k_pe; J.v = v;
   J.kv_len = kv_len;
+  J.key_mask = key_mask;
   J.B = B; J.H = H; J.Tq = Tq; J.Tk = Tk; J.past_len = past_len;
   J.scale = (double)softmax_scale;
   J.rows = rows; J.n_rows = n_rows; J.mode = mode; J.out = out; J.wsum = wsum;
@@ -273,7 +278,26 @@ int mla_oracle_rows(const uint16_t* q_nope, const uint16_t* q_pe, const uint16_t
                     const int64_t* rows, int64_t n_rows, int mode, int nthreads, double* out,
                     double* wsum) {
   return rows_impl(q_nope, q_pe, k_nope, k_pe, v, kv_len, B, H, Tq, Tk, past_len, softmax_scale,
-                   rows, n_rows, mode, nthreads, out, wsum, NULL, 1.0);
+                   rows, n_rows, mode, nthreads, out, wsum, NULL, 1.0, NULL);
+}
+
+/*
+ * The same rows with a 2D padding mask on the keys (the attention_mask argument of the
+ * model, "Kimi K2 · Causal mask", §Construct causal mask: expanded to 4D and merged with the
+ * causal mask before the scores): key_mask [B][Tk] bytes, 0 = hidden.  A hidden key gets
+ * the same additive minimum as a causally hidden one.  A row whose keys are all hidden then
+ * has every score equal to that minimum (the score is absorbed: |s| is far below the
+ * spacing of doubles near 3.4e38), so its weights are uniform over all Tk keys, as in the
+ * eager computation.
+ */
+int mla_oracle_rows_mask(const uint16_t* q_nope, const uint16_t* q_pe, const uint16_t* k_nope,
+                         const uint16_t* k_pe, const uint16_t* v, const int32_t* kv_len,
+                         const uint8_t* key_mask, int64_t B, int64_t H, int64_t Tq, int64_t Tk,
+                         int64_t past_len, float softmax_scale, const int64_t* rows,
+                         int64_t n_rows, int mode, int nthreads, double* out, double* wsum) {
+  if (!key_mask) return 15;
+  return rows_impl(q_nope, q_pe, k_nope, k_pe, v, kv_len, B, H, Tq, Tk, past_len, softmax_scale,
+                   rows, n_rows, mode, nthreads, out, wsum, NULL, 1.0, key_mask);
 }
 
 /*
@@ -290,7 +314,7 @@ int mla_oracle_rows_rope(const uint16_t* q_nope, const uint16_t* q_pe, const uin
                          double* out, const double* inv_freq, double mscale) {
   if (!inv_freq) return 14;
   return rows_impl(q_nope, q_pe, k_nope, k_pe, v, kv_len, B, H, Tq, Tk, past_len, softmax_scale,
-                   rows, n_rows, 0, nthreads, out, NULL, inv_freq, mscale);
+                   rows, n_rows, 0, nthreads, out, NULL, inv_freq, mscale, NULL);
 }
 
 /*

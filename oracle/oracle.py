@@ -58,6 +58,10 @@ def _load():
             lib.mla_oracle_rows.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, i64,
                                             ctypes.c_float, p, i64, ctypes.c_int, ctypes.c_int,
                                             p, p]
+            lib.mla_oracle_rows_mask.restype = ctypes.c_int
+            lib.mla_oracle_rows_mask.argtypes = [p, p, p, p, p, p, p, i64, i64, i64, i64, i64,
+                                                 ctypes.c_float, p, i64, ctypes.c_int,
+                                                 ctypes.c_int, p, p]
             lib.mla_oracle_round_bf16.restype = ctypes.c_double
             lib.mla_oracle_round_bf16.argtypes = [ctypes.c_double]
             lib.mla_oracle_rows_rope.restype = ctypes.c_int
@@ -95,11 +99,12 @@ def _threads(n):
 
 def oracle_rows(q_nope, q_pe, k_nope, k_pe_shared, v, kv_len, past_len: int,
                 softmax_scale: float, rows=None, mode: str = "exact", threads: int | None = None,
-                return_wsum: bool = False):
+                return_wsum: bool = False, key_mask=None):
     """Exact fp64 output rows.
 
     Shapes: q_nope [B,H,Tq,128], q_pe [B,H,Tq,64], k_nope [B,H,Tk,128],
-    k_pe_shared [B,Tk,64], v [B,H,Tk,128] (bf16), kv_len [B] int32 or None.
+    k_pe_shared [B,Tk,64], v [B,H,Tk,128] (bf16), kv_len [B] int32 or None,
+    key_mask [B,Tk] (nonzero = key visible) or None.
     rows: flat indices (b*H + h)*Tq + i, or None for all rows in that order.
     Returns float64 [n_rows,128] (and the per-row weight sum if asked).
     """
@@ -122,9 +127,18 @@ def oracle_rows(q_nope, q_pe, k_nope, k_pe_shared, v, kv_len, past_len: int,
     wsum = np.empty((n,), dtype=np.float64)
     m = {"exact": 0, "eager": 1}[mode]
     ptr = lambda a: None if a is None else a.ctypes.data  # noqa: E731
-    rc = lib.mla_oracle_rows(ptr(qn), ptr(qr), ptr(kn), ptr(kr), ptr(vv), ptr(kvl),
-                             B, H, Tq, Tk, int(past_len), float(softmax_scale), ptr(rows_arr), n,
-                             m, _threads(threads), ptr(out), ptr(wsum))
+    if key_mask is None:
+        rc = lib.mla_oracle_rows(ptr(qn), ptr(qr), ptr(kn), ptr(kr), ptr(vv), ptr(kvl),
+                                 B, H, Tq, Tk, int(past_len), float(softmax_scale),
+                                 ptr(rows_arr), n, m, _threads(threads), ptr(out), ptr(wsum))
+    else:
+        if hasattr(key_mask, "numpy"):
+            key_mask = key_mask.cpu().numpy()
+        km = np.ascontiguousarray((np.asarray(key_mask) != 0).astype(np.uint8).reshape(B, Tk))
+        rc = lib.mla_oracle_rows_mask(ptr(qn), ptr(qr), ptr(kn), ptr(kr), ptr(vv), ptr(kvl),
+                                      ptr(km), B, H, Tq, Tk, int(past_len),
+                                      float(softmax_scale), ptr(rows_arr), n, m,
+                                      _threads(threads), ptr(out), ptr(wsum))
     if rc != 0:
         raise ValueError(f"oracle rejected its arguments (code {rc})")
     return (out, wsum) if return_wsum else out

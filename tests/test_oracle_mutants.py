@@ -44,6 +44,16 @@ ROPE_MUTANTS = {
 }
 
 
+# Mistakes in the 2D padding mask, checked against the mask pins.
+MASK_MUTANTS = {
+    "mask_ignored": ("(!J->key_mask || J->key_mask[b * J->Tk + j] != 0)", "1"),
+    "mask_inverted": ("J->key_mask[b * J->Tk + j] != 0", "J->key_mask[b * J->Tk + j] == 0"),
+    "mask_wrong_sequence": ("J->key_mask[b * J->Tk + j]", "J->key_mask[j]"),
+    "hidden_keys_dropped": ("sj += visible ? 0.0 : MASK_MIN_BF16;",
+                            "sj = visible ? sj : -INFINITY;"),
+}
+
+
 def _run_pins(name, old, new, tmp_path, pin_file):
     src = open(SRC).read()
     assert old in src, f"mutation site for {name} not found"
@@ -69,3 +79,9 @@ def test_pins_kill_mutant(name, tmp_path):
 def test_rope_pins_kill_mutant(name, tmp_path):
     old, new = ROPE_MUTANTS[name]
     _run_pins(name, old, new, tmp_path, "test_oracle_rope.py")
+
+
+@pytest.mark.parametrize("name", sorted(MASK_MUTANTS))
+def test_mask_pins_kill_mutant(name, tmp_path):
+    old, new = MASK_MUTANTS[name]
+    _run_pins(name, old, new, tmp_path, "test_oracle_mask.py")
