@@ -157,6 +157,31 @@ MLA_API mla_status mla_attn_append_fwd(const uint16_t* q_nope, const uint16_t* q
                                        void* cuda_stream);
 
 /*
+ * Attention with a 2D padding mask on the keys.  The model's attention_mask ("Kimi K2 ·
+ * Causal mask", section "Construct causal mask") is expanded to 4D and merged with the
+ * causal mask, so a hidden key gets the same additive minimum as a causally hidden one:
+ *
+ *   key j is visible to query i of sequence b iff j <= i + past_len, j < kv_len[b] and
+ *   key_mask[b * Tk + j] != 0
+ *
+ * key_mask: [B, Tk] bytes in device memory (any alignment), nonzero = attend.  Left
+ * padding (a run of zeros first) and arbitrary holes are both expressible.  A query row
+ * that sees no visible key at all has every score equal to the minimum, so its weights
+ * are uniform over all Tk keys: its output is the mean of the Tk value rows (the eager
+ * result; such rows are usually padding queries).  The other arguments are those of
+ * mla_attn_fwd; the workspace must hold mla_attn_masked_workspace_bytes(B, H, Tq, Tk)
+ * bytes (for Tq > 1 it also holds the mask packed to bits).  MLA_ERR_NULL without key_mask.
+ */
+MLA_API size_t mla_attn_masked_workspace_bytes(int B, int H, int Tq, int Tk);
+MLA_API mla_status mla_attn_masked_fwd(const uint16_t* q_nope, const uint16_t* q_pe,
+                                       const uint16_t* k_nope, const uint16_t* k_pe_shared,
+                                       const uint16_t* v, const int32_t* kv_len,
+                                       const uint8_t* key_mask, int B, int H, int Tq, int Tk,
+                                       int past_len, float softmax_scale, uint16_t* out,
+                                       void* workspace, size_t workspace_bytes,
+                                       void* cuda_stream);
+
+/*
  * Rotary embedding.  The attention excerpt on "Kimi K2 · Similarities" rotates the query's
  * and the new keys' rotary parts before the cache update (rotary_emb gives cos and sin for
  * the positions, apply_rotary_pos_emb rotates q_pe and k_pe), and the rope_scaling block of

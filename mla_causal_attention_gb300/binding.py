@@ -64,7 +64,8 @@ class _Options(ctypes.Structure):
 EXPORTED = ("mla_attn_workspace_bytes", "mla_attn_fwd", "mla_attn_fwd_ex",
             "mla_attn_get_status", "mla_status_string", "mla_attn_decode_plan",
             "mla_attn_append_fwd", "mla_rope_frequencies", "mla_rope_table",
-            "mla_attn_rope_workspace_bytes", "mla_attn_rope_append_fwd")
+            "mla_attn_rope_workspace_bytes", "mla_attn_rope_append_fwd",
+            "mla_attn_masked_workspace_bytes", "mla_attn_masked_fwd")
 
 
 def library():
@@ -95,6 +96,10 @@ def library():
         lib.mla_attn_append_fwd.restype = i
         lib.mla_attn_append_fwd.argtypes = [p, p, p, p, p, p, p, p, p, i, i, i, i, i, f, p, p,
                                             sz, p]
+        lib.mla_attn_masked_workspace_bytes.restype = sz
+        lib.mla_attn_masked_workspace_bytes.argtypes = [i, i, i, i]
+        lib.mla_attn_masked_fwd.restype = i
+        lib.mla_attn_masked_fwd.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, f, p, p, sz, p]
         lib.mla_rope_frequencies.restype = i
         lib.mla_rope_frequencies.argtypes = [ctypes.POINTER(RopeConfig),
                                              ctypes.POINTER(ctypes.c_double),
@@ -265,6 +270,45 @@ def mla_attn_append_fwd(q_nope, q_pe, k_nope_new, k_pe_new, v_new, k_nope_cache,
                                      _ptr(ws), ws.numel(), ctypes.c_void_p(s.cuda_stream))
     if rc != 0:
         raise MlaAttnError(rc, "mla_attn_append_fwd: ")
+    return out
+
+
+def mla_attn_masked_fwd(q_nope, q_pe, k_nope, k_pe_shared, v, kv_len, key_mask,
+                        past_len: int, softmax_scale: float, out=None,
+                        workspace: "Workspace | None" = None, stream=None):
+    """Attention with a 2D padding mask on the keys: key_mask [B, Tk] (uint8 or bool CUDA
+    tensor, nonzero = attend).  Rows that see no visible key get the mean of all value
+    rows (uniform weights)."""
+    lib = library()
+    dev = q_nope.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    B, H, Tq = q_nope.shape[:3]
+    Tk = k_nope.shape[2]
+    bf = torch.bfloat16
+    _check(q_nope, "q_nope", bf, (B, H, Tq, 128), dev)
+    _check(q_pe, "q_pe", bf, (B, H, Tq, 64), dev)
+    _check(k_nope, "k_nope", bf, (B, H, Tk, 128), dev)
+    _check(k_pe_shared, "k_pe_shared", bf, (B, Tk, 64), dev)
+    _check(v, "v", bf, (B, H, Tk, 128), dev)
+    if kv_len is not None:
+        _check(kv_len, "kv_len", torch.int32, (B,), dev)
+    if key_mask.dtype == torch.bool:
+        key_mask = key_mask.view(torch.uint8)
+    _check(key_mask, "key_mask", torch.uint8, (B, Tk), dev)
+    if out is None:
+        out = torch.empty((B, H, Tq, 128), dtype=bf, device=dev)
+    _check(out, "out", bf, (B, H, Tq, 128), dev)
+    ws = (workspace or _default_workspace(dev)).get(
+        lib.mla_attn_masked_workspace_bytes(B, H, Tq, Tk))
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        rc = lib.mla_attn_masked_fwd(_ptr(q_nope), _ptr(q_pe), _ptr(k_nope), _ptr(k_pe_shared),
+                                     _ptr(v), _ptr(kv_len), _ptr(key_mask), B, H, Tq, Tk,
+                                     int(past_len), float(softmax_scale), _ptr(out), _ptr(ws),
+                                     ws.numel(), ctypes.c_void_p(s.cuda_stream))
+    if rc != 0:
+        raise MlaAttnError(rc, "mla_attn_masked_fwd: ")
     return out
 
 

@@ -4,7 +4,8 @@
 //   s_j = softmax_scale * ([q_nope | q_pe] . [k_nope[b,h,j] | k_pe_shared[b,j]])
 //   out = sum_j softmax(s)_j v[b,h,j]
 // (the attention excerpt on "Kimi K2 · Similarities"; with Tq = 1 and Tk = past_len + 1
-// the causal limit admits every cached key, so only kv_len hides keys).
+// the causal limit admits every cached key, so only kv_len, and the optional 2D padding
+// mask on keys, hide keys).
 //
 // Work split: one CTA per (group of 4 heads, key chunk, sequence).  One producer thread
 // streams each 32-key stage with 1-D bulk copies into a 3-deep shared-memory ring: the
@@ -80,7 +81,9 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-template <int G, int T, int NST, int WPH, int MINB>
+// KM: the 2D padding mask on keys is applied (p.key_mask); a separate instantiation so the
+// unmasked kernel carries none of its per-key work.
+template <int G, int T, int NST, int WPH, int MINB, bool KM>
 __global__ void __launch_bounds__(DecCfg<G, T, NST, WPH>::kThreads, MINB)
     decode_splitkv_kernel(const DecodeArgs p) {
   using C = DecCfg<G, T, NST, WPH>;
@@ -206,9 +209,16 @@ __global__ void __launch_bounds__(DecCfg<G, T, NST, WPH>::kThreads, MINB)
 
   for (int it = 0; it < n_tiles; ++it) {
     const int slot = it % NST;
-    if (!mbar_wait(&full[slot], (it / NST) & 1, p.status, abort_flag)) break;
     const int jt = j0 + it * T;
     const int nt = min(T, j1 - jt);
+    // 2D padding mask: this lane's keys' bytes, fetched before the stage wait.
+    bool hidden[C::kPasses];
+#pragma unroll
+    for (int ps = 0; ps < C::kPasses; ++ps) {
+      const int t = wh * C::kTokPerWarp + ps * 4 + tk;
+      hidden[ps] = KM && t < nt && p.key_mask[(size_t)b * p.Tk + jt + t] == 0;
+    }
+    if (!mbar_wait(&full[slot], (it / NST) & 1, p.status, abort_flag)) break;
     if (head_ok) {
       const uint8_t* st = stages + slot * C::kStageBytes;
       const uint8_t* kpe_s = st;
@@ -227,7 +237,7 @@ __global__ void __launch_bounds__(DecCfg<G, T, NST, WPH>::kThreads, MINB)
         d += __shfl_xor_sync(0xffffffffu, d, 1);
         d += __shfl_xor_sync(0xffffffffu, d, 2);
         d += __shfl_xor_sync(0xffffffffu, d, 4);
-        sc[ps] = (t < nt) ? d : -INFINITY;
+        sc[ps] = (t < nt && !hidden[ps]) ? d : -INFINITY;
       }
       float mx = sc[0];
 #pragma unroll
@@ -294,7 +304,8 @@ __global__ void __launch_bounds__(DecCfg<G, T, NST, WPH>::kThreads, MINB)
     o[3] += f * a.w;
   }
   if (p.splits == 1) {
-    const float inv = 1.f / l;
+    // l = 0 only when the 2D padding mask hides every key; that row is rewritten later.
+    const float inv = l > 0.f ? 1.f / l : 0.f;
     uint2 w;
     w.x = pack_bf16x2(o[0] * inv, o[1] * inv);
     w.y = pack_bf16x2(o[2] * inv, o[3] * inv);
@@ -358,18 +369,18 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeArgs p)
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-  const float inv = 1.f / l;
+  const float inv = l > 0.f ? 1.f / l : 0.f;  // see the single-split case
   uint2 o;
   o.x = pack_bf16x2(acc.x * inv, acc.y * inv);
   o.y = pack_bf16x2(acc.z * inv, acc.w * inv);
   *reinterpret_cast<uint2*>(p.out + (size_t)w * 128 + lane * 4) = o;
 }
 
-template <int T, int MINB>
+template <int T, int MINB, bool KM>
 cudaError_t launch_split(const DecodeArgs& a, cudaStream_t stream) {
   constexpr int G = kDecHeadsPerCta, NST = 3, WPH = 2;
   using C = DecCfg<G, T, NST, WPH>;
-  auto kern = decode_splitkv_kernel<G, T, NST, WPH, MINB>;
+  auto kern = decode_splitkv_kernel<G, T, NST, WPH, MINB, KM>;
   static std::atomic<uint64_t> attr_done{0};  // bit per device: smem attribute set
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -391,8 +402,13 @@ cudaError_t launch_split(const DecodeArgs& a, cudaStream_t stream) {
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   // Large problems: 32-key stages, 1 CTA per SM (213 KB of stages in flight per SM).
   // Small problems: 16-key stages, 2 CTAs per SM, so the grid fits in one wave.
-  cudaError_t e = a.small ? launch_split<kDecTokensPerStage / 2, 2>(a, stream)
-                          : launch_split<kDecTokensPerStage, 1>(a, stream);
+  cudaError_t e;
+  if (a.key_mask)
+    e = a.small ? launch_split<kDecTokensPerStage / 2, 2, true>(a, stream)
+                : launch_split<kDecTokensPerStage, 1, true>(a, stream);
+  else
+    e = a.small ? launch_split<kDecTokensPerStage / 2, 2, false>(a, stream)
+                : launch_split<kDecTokensPerStage, 1, false>(a, stream);
   if (e != cudaSuccess || a.splits == 1) return e;
   // The combine pass is a programmatic dependent launch: its launch latency overlaps
   // the tail of the split kernel.

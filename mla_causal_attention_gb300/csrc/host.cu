@@ -68,6 +68,11 @@ size_t decode_workspace(int B, int H, int splits) {
          (size_t)B * H * splits * 128 * sizeof(float);
 }
 
+// Packed 2D padding mask for the prefill kernel: [B][ceil(Tk/128)][4] words.
+size_t key_bits_bytes(int B, int Tk) {
+  return ((size_t)B * ((Tk + 127) / 128) * 16 + 255) & ~(size_t)255;
+}
+
 // Rotary workspace: rotated queries [B,H,Tq,64] then rotated new rotary keys [B,Tq,64],
 // each on a 256-byte boundary, after the attention call's own workspace.
 size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -169,6 +174,15 @@ size_t mla_attn_workspace_bytes(int B, int H, int Tq, int Tk) {
 namespace mla {
 namespace {
 
+mla_status launch_fixup(const uint8_t* key_mask, const int32_t* kv_len, const uint16_t* v,
+                        uint16_t* out, int B, int H, int Tq, int Tk, int past_len, int kv_rows,
+                        cudaStream_t stream) {
+  FixupArgs f;
+  f.key_mask = key_mask; f.kv_len = kv_len; f.v = v; f.out = out;
+  f.B = B; f.H = H; f.Tq = Tq; f.Tk = Tk; f.past_len = past_len; f.kv_rows = kv_rows;
+  return launch_masked_rows_fixup(f, stream) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
 struct AppendPtrs {
   const uint16_t* new_k_nope;
   const uint16_t* new_k_pe;
@@ -180,13 +194,15 @@ struct AppendPtrs {
 
 // Argument checks and launch shared by the attention entry points.  kv_rows is the row
 // stride of the key/value buffers (>= Tk); app (decode only) fuses the cache append;
-// check_only runs every check and returns without launching.
+// check_only runs every check and returns without launching; key_mask (may be null) is the
+// 2D padding mask [B][Tk] on keys.
 mla_status attention_impl(const uint16_t* q_nope, const uint16_t* q_pe, const uint16_t* k_nope,
                           const uint16_t* k_pe_shared, const uint16_t* v, const int32_t* kv_len,
                           int B, int H, int Tq, int Tk, int past_len, float softmax_scale,
                           uint16_t* out, void* workspace, size_t workspace_bytes,
                           void* cuda_stream, const mla_attn_options* options, int kv_rows,
-                          const AppendPtrs* app, bool check_only = false) {
+                          const AppendPtrs* app, bool check_only = false,
+                          const uint8_t* key_mask = nullptr) {
   if (!q_nope || !q_pe || !k_nope || !k_pe_shared || !v || !out) return MLA_ERR_NULL;
   if (!workspace) return MLA_ERR_WORKSPACE;
   mla_status st = check_shape(B, H, Tq, Tk, past_len);
@@ -234,18 +250,36 @@ mla_status attention_impl(const uint16_t* q_nope, const uint16_t* q_pe, const ui
       a.cache_k_nope = app->cache_k_nope; a.cache_k_pe = app->cache_k_pe;
       a.cache_v = app->cache_v;
     }
-    return launch_decode(a, stream) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+    a.key_mask = key_mask;
+    if (launch_decode(a, stream) != cudaSuccess) return MLA_ERR_CUDA;
+    return key_mask ? launch_fixup(key_mask, kv_len, v, out, B, H, Tq, Tk, past_len, kv_rows,
+                                   stream)
+                    : MLA_OK;
   }
 
-  if (workspace_bytes < kStatusBytes) return MLA_ERR_WORKSPACE;
+  const size_t need = kStatusBytes + (key_mask ? key_bits_bytes(B, Tk) : 0);
+  if (workspace_bytes < need) return MLA_ERR_WORKSPACE;
   if (check_only) return MLA_OK;
+  uint32_t* key_bits = nullptr;
+  if (key_mask) {
+    KeyBitsArgs kb;
+    kb.key_mask = key_mask;
+    kb.bits = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + kStatusBytes);
+    kb.B = B; kb.Tk = Tk; kb.n_kt = (Tk + 127) / 128;
+    if (launch_key_bits(kb, stream) != cudaSuccess) return MLA_ERR_CUDA;
+    key_bits = kb.bits;
+  }
   PrefillArgs a{};
   a.q_nope = q_nope; a.q_pe = q_pe; a.k_nope = k_nope; a.k_pe = k_pe_shared; a.v = v;
   a.kv_len = kv_len; a.out = out; a.status = status;
   a.B = B; a.H = H; a.Tq = Tq; a.Tk = Tk; a.past_len = past_len;
   a.scale_log2 = scale_log2;
   a.kv_rows = kv_rows;
-  return launch_prefill(a, stream) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+  a.key_bits = key_bits;
+  if (launch_prefill(a, stream) != cudaSuccess) return MLA_ERR_CUDA;
+  return key_mask ? launch_fixup(key_mask, kv_len, v, out, B, H, Tq, Tk, past_len, kv_rows,
+                                 stream)
+                  : MLA_OK;
 }
 
 }  // namespace
@@ -384,6 +418,24 @@ mla_status mla_attn_rope_append_fwd(const uint16_t* q_nope, const uint16_t* q_pe
   return attention_impl(q_nope, q_pe_rot, k_nope_cache, k_pe_cache, v_cache, kv_len, B, H, Tq,
                         Tk, past_len, softmax_scale, out, workspace, workspace_bytes,
                         cuda_stream, nullptr, T_cap, fused);
+}
+
+size_t mla_attn_masked_workspace_bytes(int B, int H, int Tq, int Tk) {
+  const size_t base = mla_attn_workspace_bytes(B, H, Tq, Tk);
+  if (base == 0) return 0;
+  return Tq == 1 ? base : kStatusBytes + key_bits_bytes(B, Tk);
+}
+
+mla_status mla_attn_masked_fwd(const uint16_t* q_nope, const uint16_t* q_pe,
+                               const uint16_t* k_nope, const uint16_t* k_pe_shared,
+                               const uint16_t* v, const int32_t* kv_len,
+                               const uint8_t* key_mask, int B, int H, int Tq, int Tk,
+                               int past_len, float softmax_scale, uint16_t* out,
+                               void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  if (!key_mask) return MLA_ERR_NULL;
+  return attention_impl(q_nope, q_pe, k_nope, k_pe_shared, v, kv_len, B, H, Tq, Tk, past_len,
+                        softmax_scale, out, workspace, workspace_bytes, cuda_stream, nullptr, Tk,
+                        nullptr, false, key_mask);
 }
 
 mla_status mla_attn_fwd(const uint16_t* q_nope, const uint16_t* q_pe, const uint16_t* k_nope,

@@ -37,6 +37,8 @@ struct DecodeArgs {
   uint16_t* cache_k_nope;
   uint16_t* cache_k_pe;
   uint16_t* cache_v;
+  // Optional 2D padding mask [B][Tk] (0 = key hidden); null otherwise.
+  const uint8_t* key_mask;
 };
 
 // Decode kernel configuration (shared with the scheduler).
@@ -68,6 +70,9 @@ struct PrefillArgs {
   int B, H, Tq, Tk, past_len;
   float scale_log2;
   int kv_rows;  // rows per (b, h) of k_nope / v and per b of k_pe (>= Tk)
+  // Optional 2D padding mask packed by launch_key_bits: [B][ceil(Tk/128)][4] words, bit e
+  // of word c of key tile t = visibility of key 128 t + 32 c + e.  Null: no mask.
+  const uint32_t* key_bits;
 };
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);
@@ -110,6 +115,24 @@ struct RopeAppendArgs {
   int B, H, Tq, past_len, kv_rows;
 };
 cudaError_t launch_rope_append(const RopeAppendArgs& a, cudaStream_t stream);
+
+// Packing of the 2D padding mask for the prefill kernel.
+struct KeyBitsArgs {
+  const uint8_t* key_mask;  // [B][Tk]
+  uint32_t* bits;           // [B][n_kt][4]
+  int B, Tk, n_kt;
+};
+cudaError_t launch_key_bits(const KeyBitsArgs& a, cudaStream_t stream);
+
+// Rows that see no visible key under the 2D padding mask: out = mean of all Tk value rows.
+struct FixupArgs {
+  const uint8_t* key_mask;  // [B][Tk]
+  const int32_t* kv_len;    // may be null
+  const uint16_t* v;        // [B][H][kv_rows][128]
+  uint16_t* out;            // [B][H][Tq][128]
+  int B, H, Tq, Tk, past_len, kv_rows;
+};
+cudaError_t launch_masked_rows_fixup(const FixupArgs& a, cudaStream_t stream);
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();

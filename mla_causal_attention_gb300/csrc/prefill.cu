@@ -64,9 +64,10 @@ struct PrefillParams {
   CUtensorMap tm_kr;  // k_pe    {64,  Tk, B}
   CUtensorMap tm_v;   // v       {128, Tk, B*H}
   const int32_t* kv_len;
+  const uint32_t* key_bits;  // packed 2D padding mask [B][n_kt][4], or null
   uint16_t* out;
   int* status;
-  int B, H, Tq, Tk, past_len, n_qb;
+  int B, H, Tq, Tk, past_len, n_qb, n_kt;
   float scale_log2;
 };
 
@@ -175,6 +176,9 @@ __device__ __forceinline__ Unit unit_make(const PrefillParams& p, int unit, int 
   return w;
 }
 
+// kMasked: the 2D padding mask on keys is applied (p.key_bits); a separate instantiation so
+// the unmasked kernel carries none of its per-tile work.
+template <bool kMasked>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_prefill_kernel(const __grid_constant__ PrefillParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -467,6 +471,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m = -INFINITY;
       float l = 0.f;
       for (int j = 0; j < ntt; ++j, ++st) {
+        // 2D padding mask bits of this key tile (same for every row of the CTA), fetched
+        // before the wait so the load overlaps it.
+        uint4 kbits = make_uint4(~0u, ~0u, ~0u, ~0u);
+        if (kMasked)
+          kbits = *reinterpret_cast<const uint4*>(p.key_bits +
+                                                  ((size_t)w.b * p.n_kt + j) * 4);
         ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], st & 1, p.status, abort_flag));
         if (!ok) break;
         tc::fence_after_sync();
@@ -484,6 +494,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 0; e < 32; ++e)
               if (jt + c * 32 + e >= limit) r[c][e] = __float_as_uint(-INFINITY);
+        }
+        if (kMasked && (kbits.x & kbits.y & kbits.z & kbits.w) != ~0u) {
+          const uint32_t kw[4] = {kbits.x, kbits.y, kbits.z, kbits.w};
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (!((kw[c] >> e) & 1u)) r[c][e] = __float_as_uint(-INFINITY);
         }
         // Row max: 8 independent chains of three-input maxima (64 instructions for 128
         // scores; a single 128-long chain would be latency-bound).
@@ -523,8 +541,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // p = 2^(s * scale * log2(e) - m): the scale-and-subtract and the row sum run on
         // fp32 pairs (one instruction per two scores), the exponentials on the MUFU.
+        // While every key so far is hidden (only under a 2D padding mask) the running max is
+        // -inf; exponents are then taken against 0, giving exactly 0 for hidden keys.
+        const float m_base = (kMasked && m == -INFINITY) ? 0.f : m;
         const uint64_t sl2_2 = f2_pack(sl2, sl2);
-        const uint64_t negm_2 = f2_pack(-m, -m);
+        const uint64_t negm_2 = f2_pack(-m_base, -m_base);
         uint64_t sp2[4] = {0ull, 0ull, 0ull, 0ull};
         uint32_t pk[2][32];
 #pragma unroll
@@ -571,7 +592,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc::fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars->o_free[t]);
-      const float inv = 1.0f / l;
+      // l = 0 only when the 2D padding mask hides every key of the row; that row is
+      // rewritten afterwards as the mean of all value rows.
+      const float inv = l > 0.f ? 1.0f / l : 0.f;
       if (qi < p.Tq) {
         uint16_t* row = p.out + ((size_t)w.bh * p.Tq + qi) * 128;
         auto pk = [&](int c, int e) {
@@ -755,6 +778,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   if (!tensor_maps(a, &p)) return cudaErrorInvalidValue;
   const uint64_t BH = (uint64_t)a.B * a.H;
   p.kv_len = a.kv_len;
+  p.key_bits = a.key_bits;
+  p.n_kt = (a.Tk + kBN - 1) / kBN;
   p.out = a.out;
   p.status = a.status;
   p.B = a.B;
@@ -772,15 +797,21 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (attr_device != dev) {
-    e = cudaFuncSetAttribute(mla_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes);
+    e = cudaFuncSetAttribute(mla_prefill_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(mla_prefill_kernel<true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_device = dev;
   }
   // Persistent: one CTA per SM (at most one per unit), each walking its units.
   const int sms = device_sm_count();
   const uint64_t grid = std::min<uint64_t>(units, (uint64_t)(sms > 0 ? sms : 152));
-  mla_prefill_kernel<<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(p);
+  if (p.key_bits)
+    mla_prefill_kernel<true><<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(p);
+  else
+    mla_prefill_kernel<false><<<(unsigned)grid, kThreads, kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -117,3 +117,24 @@ def test_binding_refuses_cpu_tensors(lib):
     x = torch.zeros(1, 1, 2, 128, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         binding.mla_attn_fwd(x, x, x, x, x, None, 0, 0.1)
+
+
+def test_masked_entry_host_errors(lib):
+    buf = (ctypes.c_uint8 * 4096)()
+    base = (ctypes.addressof(buf) + 255) & ~255
+    P = [ctypes.c_void_p(base + 256 * i) for i in range(9)]
+    S = binding.MlaStatus
+    q, qr, k, kr, v, km, out, ws = P[:8]
+    call = lambda km_, B=1, Tq=2, Tk=2, past=0, wsb=4096: lib.mla_attn_masked_fwd(  # noqa
+        q, qr, k, kr, v, None, km_, B, 1, Tq, Tk, past, 0.1, out, ws, wsb, None)
+    assert call(None) == S.ERR_NULL
+    assert call(km, Tk=3) == S.ERR_SHAPE
+    import torch
+    # prefill needs room for the packed mask (checked after the device check)
+    want = (S.ERR_WORKSPACE,) if torch.cuda.is_available() else (S.ERR_CUDA, S.ERR_DEVICE)
+    assert call(km, wsb=256) in want
+    assert lib.mla_attn_masked_workspace_bytes(2, 4, 130, 207) == 256 + 256
+    assert lib.mla_attn_masked_workspace_bytes(3, 8, 1, 300) == \
+        lib.mla_attn_workspace_bytes(3, 8, 1, 300)
+    if not torch.cuda.is_available():
+        assert call(km) in (S.ERR_CUDA, S.ERR_DEVICE)
