@@ -83,6 +83,8 @@ typedef struct {
   const uint16_t *q_nope, *q_pe, *k_nope, *k_pe, *v;
   const int32_t* kv_len;
   const uint8_t* key_mask; /* [B][Tk], 0 = key hidden; NULL = no 2D padding mask */
+  const uint16_t* c_kv;    /* latent rows [B][Tk][512]; NULL = per-head k_nope / v given */
+  const uint16_t* w_kvb;   /* kv_b_proj weight [H*256][512] (latent mode) */
   int64_t B, H, Tq, Tk, past_len;
   double scale;
   const int64_t* rows;
@@ -110,8 +112,66 @@ static void rotate64(double* y, const double* x, double pos, const double* f, do
   }
 }
 
+#define D_LAT 512 /* kv_lora_rank */
+
+/* One output row from the latent cache, in the pages' (non-absorbed) form: kv_b_proj maps
+ * the latent row c_j of key j to 64 x (128 + 128) features; head h takes features
+ * [256h, 256h + 128) as its no-rope key and [256h + 128, 256h + 256) as its value.  Then
+ * the same concat, scores, mask and softmax as one_row.  s is scratch of Tk doubles;
+ * kv is scratch of 256 doubles. */
+static int one_row_latent(const job_t* J, int64_t flat, double* s, double* o) {
+  const int64_t i = flat % J->Tq;
+  const int64_t bh = flat / J->Tq;
+  const int64_t b = bh / J->H;
+  const int64_t h = bh % J->H;
+  if (b >= J->B) return 1;
+  const int64_t kvl = J->kv_len ? (int64_t)J->kv_len[b] : J->Tk;
+  if (kvl < 1 || kvl > J->Tk) return 2;
+  double q[D_NOPE + D_ROPE];
+  for (int d = 0; d < D_NOPE; ++d) q[d] = bf16_to_double(J->q_nope[(bh * J->Tq + i) * D_NOPE + d]);
+  for (int d = 0; d < D_ROPE; ++d) q[D_NOPE + d] = bf16_to_double(J->q_pe[(bh * J->Tq + i) * D_ROPE + d]);
+  const uint16_t* wk = J->w_kvb + (h * 256) * D_LAT;        /* rows of the no-rope key */
+  const uint16_t* wv = J->w_kvb + (h * 256 + 128) * D_LAT;  /* rows of the value */
+  for (int64_t j = 0; j < J->Tk; ++j) {
+    const uint16_t* c = J->c_kv + (b * J->Tk + j) * D_LAT;
+    double acc = 0.0;
+    for (int e = 0; e < D_NOPE; ++e) {
+      double kn = 0.0; /* k_nope[b, h, j, e] = sum_d W[256h + e, d] c[d] */
+      for (int d = 0; d < D_LAT; ++d) kn += bf16_to_double(wk[e * D_LAT + d]) * bf16_to_double(c[d]);
+      acc += q[e] * kn;
+    }
+    const uint16_t* kr = J->k_pe + (b * J->Tk + j) * D_ROPE;
+    for (int d = 0; d < D_ROPE; ++d) acc += q[D_NOPE + d] * bf16_to_double(kr[d]); /* shared rotary key */
+    double sj = acc * J->scale;
+    const int visible = (j <= i + J->past_len) && (j < kvl);
+    sj += visible ? 0.0 : MASK_MIN_BF16;
+    s[j] = sj;
+  }
+  double m = s[0];
+  for (int64_t j = 1; j < J->Tk; ++j)
+    if (s[j] > m) m = s[j];
+  double denom = 0.0;
+  for (int64_t j = 0; j < J->Tk; ++j) {
+    s[j] = exp(s[j] - m);
+    denom += s[j];
+  }
+  for (int e = 0; e < D_V; ++e) o[e] = 0.0;
+  for (int64_t j = 0; j < J->Tk; ++j) {
+    const double w = s[j] / denom;
+    if (w == 0.0) continue;
+    const uint16_t* c = J->c_kv + (b * J->Tk + j) * D_LAT;
+    for (int e = 0; e < D_V; ++e) {
+      double v = 0.0; /* v[b, h, j, e] = sum_d W[256h + 128 + e, d] c[d] */
+      for (int d = 0; d < D_LAT; ++d) v += bf16_to_double(wv[e * D_LAT + d]) * bf16_to_double(c[d]);
+      o[e] += w * v;
+    }
+  }
+  return 0;
+}
+
 /* One output row o[b, h, i, :].  s is scratch of Tk doubles. */
 static int one_row(const job_t* J, int64_t flat, double* s, double* o, double* wsum_out) {
+  if (J->c_kv) return one_row_latent(J, flat, s, o);
   const int64_t i = flat % J->Tq;
   const int64_t bh = flat / J->Tq;
   const int64_t b = bh / J->H;
@@ -315,6 +375,47 @@ int mla_oracle_rows_rope(const uint16_t* q_nope, const uint16_t* q_pe, const uin
   if (!inv_freq) return 14;
   return rows_impl(q_nope, q_pe, k_nope, k_pe, v, kv_len, B, H, Tq, Tk, past_len, softmax_scale,
                    rows, n_rows, 0, nthreads, out, NULL, inv_freq, mscale, NULL);
+}
+
+/*
+ * Output rows of attention over the latent cache: c_kv [B][Tk][512] (the input of
+ * kv_b_proj), k_pe [B][Tk][64] (the shared rotary key), w_kvb [H*256][512] (the kv_b_proj
+ * weight, "Kimi K2 · Similarities", §Scale scores: kv_lora_rank -> num_heads x
+ * (qk_nope_head_dim + v_head_dim)), q_nope [B][H][Tq][128], q_pe [B][H][Tq][64].  Computed
+ * in the non-absorbed form (per-head keys and values materialised from the latent), so it
+ * checks the absorbed kernels without sharing their algebra.
+ */
+int mla_oracle_latent_rows(const uint16_t* q_nope, const uint16_t* q_pe, const uint16_t* c_kv,
+                           const uint16_t* k_pe, const uint16_t* w_kvb, const int32_t* kv_len,
+                           int64_t B, int64_t H, int64_t Tq, int64_t Tk, int64_t past_len,
+                           float softmax_scale, const int64_t* rows, int64_t n_rows, int nthreads,
+                           double* out) {
+  if (!c_kv || !w_kvb || !q_nope || !q_pe || !k_pe || !out) return 11;
+  if (B < 1 || H < 1 || Tq < 1 || Tk < 1 || past_len < 0 || Tk != past_len + Tq) return 10;
+  if (rows) {
+    for (int64_t r = 0; r < n_rows; ++r)
+      if (rows[r] < 0 || rows[r] >= B * H * Tq) return 13;
+  } else {
+    n_rows = B * H * Tq;
+  }
+  job_t J;
+  memset(&J, 0, sizeof J);
+  J.q_nope = q_nope; J.q_pe = q_pe; J.k_pe = k_pe; J.c_kv = c_kv; J.w_kvb = w_kvb;
+  J.kv_len = kv_len;
+  J.B = B; J.H = H; J.Tq = Tq; J.Tk = Tk; J.past_len = past_len;
+  J.scale = (double)softmax_scale;
+  J.rows = rows; J.n_rows = n_rows; J.out = out;
+  pthread_mutex_init(&J.lock, NULL);
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 256) nthreads = 256;
+  pthread_t th[256];
+  int started = 0;
+  for (int t = 0; t < nthreads; ++t)
+    if (pthread_create(&th[t], NULL, worker, &J) == 0) ++started;
+  if (started == 0) worker(&J);
+  for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
+  pthread_mutex_destroy(&J.lock);
+  return J.err;
 }
 
 /*

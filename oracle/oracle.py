@@ -62,6 +62,9 @@ def _load():
             lib.mla_oracle_rows_mask.argtypes = [p, p, p, p, p, p, p, i64, i64, i64, i64, i64,
                                                  ctypes.c_float, p, i64, ctypes.c_int,
                                                  ctypes.c_int, p, p]
+            lib.mla_oracle_latent_rows.restype = ctypes.c_int
+            lib.mla_oracle_latent_rows.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, i64,
+                                                   ctypes.c_float, p, i64, ctypes.c_int, p]
             lib.mla_oracle_round_bf16.restype = ctypes.c_double
             lib.mla_oracle_round_bf16.argtypes = [ctypes.c_double]
             lib.mla_oracle_rows_rope.restype = ctypes.c_int
@@ -168,6 +171,33 @@ def yarn(theta: float, factor: float, orig_max_pos: int, beta_fast: float, beta_
                         float(beta_slow), float(mscale), float(mscale_all_dim), f.ctypes.data,
                         r.ctypes.data)
     return f, float(r[0])
+
+
+def oracle_latent_rows(q_nope, q_pe, c_kv, k_pe, w_kvb, kv_len, past_len: int,
+                       softmax_scale: float, rows=None, threads: int | None = None):
+    """Output rows of attention over the latent cache, non-absorbed form, fp64.
+
+    q_nope [B,H,Tq,128], q_pe [B,H,Tq,64], c_kv [B,Tk,512], k_pe [B,Tk,64] (bf16),
+    w_kvb [H*256,512] (bf16, kv_b_proj weight), kv_len [B] or None.  Returns [n_rows,128].
+    """
+    lib = _load()
+    qn, qr, c, kr, w = (_bits(t) for t in (q_nope, q_pe, c_kv, k_pe, w_kvb))
+    B, H, Tq, _ = qn.shape
+    Tk = c.shape[1]
+    assert c.shape == (B, Tk, 512) and kr.shape == (B, Tk, 64) and w.shape == (H * 256, 512)
+    kvl = None if kv_len is None else np.ascontiguousarray(
+        np.asarray(kv_len, dtype=np.int32).reshape(B))
+    rows_arr = None if rows is None else np.ascontiguousarray(
+        np.asarray(rows, dtype=np.int64).reshape(-1))
+    n = B * H * Tq if rows is None else rows_arr.size
+    out = np.empty((n, 128), dtype=np.float64)
+    ptr = lambda a: None if a is None else a.ctypes.data  # noqa: E731
+    rc = lib.mla_oracle_latent_rows(ptr(qn), ptr(qr), ptr(c), ptr(kr), ptr(w), ptr(kvl), B, H,
+                                    Tq, Tk, int(past_len), float(softmax_scale), ptr(rows_arr),
+                                    n, _threads(threads), ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle rejected its arguments (code {rc})")
+    return out
 
 
 def rotate(x, positions, inv_freq, mscale: float):

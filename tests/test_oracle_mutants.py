@@ -54,6 +54,19 @@ MASK_MUTANTS = {
 }
 
 
+# Mistakes in the latent-cache rows, checked against the latent pins.
+LATENT_MUTANTS = {
+    "latent_key_value_swapped": ("const uint16_t* wk = J->w_kvb + (h * 256) * D_LAT;",
+                                 "const uint16_t* wk = J->w_kvb + (h * 256 + 128) * D_LAT;"),
+    "latent_head_ignored": ("const uint16_t* wv = J->w_kvb + (h * 256 + 128) * D_LAT;",
+                            "const uint16_t* wv = J->w_kvb + (128) * D_LAT;"),
+    "latent_weight_transposed": ("kn += bf16_to_double(wk[e * D_LAT + d]) * bf16_to_double(c[d]);",
+                                 "kn += bf16_to_double(wk[d * 128 + e]) * bf16_to_double(c[d]);"),
+    "latent_rope_dropped": ("acc += q[D_NOPE + d] * bf16_to_double(kr[d]); /* shared rotary key */",
+                            "acc += 0.0; /* shared rotary key */"),
+}
+
+
 def _run_pins(name, old, new, tmp_path, pin_file):
     src = open(SRC).read()
     assert old in src, f"mutation site for {name} not found"
@@ -85,3 +98,9 @@ def test_rope_pins_kill_mutant(name, tmp_path):
 def test_mask_pins_kill_mutant(name, tmp_path):
     old, new = MASK_MUTANTS[name]
     _run_pins(name, old, new, tmp_path, "test_oracle_mask.py")
+
+
+@pytest.mark.parametrize("name", sorted(LATENT_MUTANTS))
+def test_latent_pins_kill_mutant(name, tmp_path):
+    old, new = LATENT_MUTANTS[name]
+    _run_pins(name, old, new, tmp_path, "test_oracle_latent.py")
