@@ -46,6 +46,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="long_prefill")
     ap.add_argument("--secondary", default="decode_ragged")
+    ap.add_argument("--latent", default="latent_decode_ragged",
+                    help="decode over the latent cache, reported under secondary (or none)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
@@ -293,6 +295,95 @@ def measure_ours(wl, args, rank, world, local, with_cpu):
     return res
 
 
+def measure_latent(name, args, rank, world, local, with_cpu):
+    """Decode over the latent cache (absorbed kv_b_proj): GB/s of algorithmic bytes."""
+    import ctypes
+
+    import numpy as np
+    import torch
+
+    from mla_causal_attention_gb300 import binding
+    from mla_causal_attention_gb300.inputs import make_latent_inputs
+    from mla_causal_attention_gb300.workloads import LATENT_WORKLOADS, latent_algorithmic_bytes
+
+    wl = LATENT_WORKLOADS[name]
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    host = make_latent_inputs(wl, seed=args.seed + rank)
+    d = {k: v.to(dev) for k, v in host.items()}
+    out = torch.empty((wl.B, wl.H, 128), dtype=torch.bfloat16, device=dev)
+    lib = binding.library()
+    wsobj = binding.Workspace(dev)
+    ws = wsobj.get(lib.mla_latent_workspace_bytes(wl.B, wl.H, wl.Tk))
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    work = latent_algorithmic_bytes(wl, host["kv_len"].numpy())
+    P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    cargs = (P(d["q_nope"]), P(d["q_pe"]), P(d["c_kv"]), P(d["k_pe"]), P(d["w_kvb"]),
+             P(d["kv_len"]), wl.B, wl.H, wl.Tk, ctypes.c_float(wl.softmax_scale), P(out), P(ws),
+             ctypes.c_size_t(ws.numel()), ctypes.c_void_p(stream.cuda_stream))
+
+    def call():
+        rc = lib.mla_latent_decode_fwd(*cargs)
+        if rc != 0:
+            raise RuntimeError(f"mla_latent_decode_fwd returned {rc}")
+
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            starts[i].record(stream)
+            call()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = max_over_ranks(sum(step_ms), world, dev) / args.steps
+    if binding.mla_attn_get_status(wsobj, dev) != 0:
+        raise RuntimeError("device status set by the latent decode")
+    peak, peak_src = peak_for("hbm", False)
+    achieved = work / (ms * 1e-3) * 1e-9
+    res = {"workload": name, "value": whole_job_rate(work, world, ms, 1e-9), "unit": "GB/s",
+           "ms_per_step": ms, "step_ms_min": min(step_ms), "step_ms_max": max(step_ms),
+           "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                        "frac": achieved / peak, "traffic": recorded_traffic("latent_splitkv_kernel"),
+                        "peak_source": peak_src, "kernel": "latent path (4 kernels)",
+                        "algorithmic_per_launch": work},
+           "clocks": clk.summary(), "gpu_launches": 4 * args.steps,
+           "config": {"workload": name, "B": wl.B, "H": wl.H, "Tk": wl.Tk,
+                      "kv_len_range": wl.kv_len_range, "latent": 512, "rope": 64,
+                      "weights": "synthetic kv_b_proj ~ N(0, 1/512)",
+                      "l2": "flushed (2x L2 write) before every timed step, outside its events"}}
+    if with_cpu and rank == 0 and world == 1:
+        from oracle import oracle_latent_rows
+
+        rng = np.random.default_rng(args.seed)
+        kv = host["kv_len"].numpy()
+        t0 = time.perf_counter()
+        rows, n = [], 0
+        while time.perf_counter() - t0 < min(args.cpu_seconds, 5.0):
+            r = [int(x) for x in rng.integers(0, wl.B * wl.H, 16)]
+            oracle_latent_rows(host["q_nope"][:, :, None], host["q_pe"][:, :, None],
+                               host["c_kv"], host["k_pe"], host["w_kvb"], host["kv_len"],
+                               wl.Tk - 1, wl.softmax_scale, rows=r)
+            rows += r
+            n += 1
+        dt = time.perf_counter() - t0
+        per_row = sum(int(kv[x // wl.H]) * 1152 for x in rows)
+        res["cpu_baseline"] = {"value": per_row / dt * 1e-9, "unit": "GB/s",
+                               "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+                               "sample": f"{len(rows)} random output rows (non-absorbed "
+                                         f"oracle), {dt:.1f} s", "seconds": dt}
+    del flush
+    return res
+
+
 def measure_e2e(wl, host, d, out, ws, stream, m, args, world):
     """Same metric through the public API from pinned host memory, copies included."""
     import torch
@@ -470,6 +561,9 @@ def main():
         swl = WORKLOADS[args.secondary]
         sec = measure_ours(swl, args, rank, world, local, with_cpu=not args.no_cpu)
         sec["config"] = workload_config(swl, args)
+    lat = None
+    if args.latent and args.latent != "none":
+        lat = measure_latent(args.latent, args, rank, world, local, with_cpu=not args.no_cpu)
     if rank == 0:
         m = workload_metrics(wl, [wl.Tk] * wl.B)
         line = base_line(args, wl, m, res["value"], res["ms_per_step"])
@@ -482,6 +576,8 @@ def main():
         if sec is not None:
             line["secondary"] = [{"workload": args.secondary, **{k: v for k, v in sec.items()
                                                                 if k != "work_per_step"}}]
+        if lat is not None:
+            line.setdefault("secondary", []).append(lat)
         print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()

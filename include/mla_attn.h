@@ -182,6 +182,39 @@ MLA_API mla_status mla_attn_masked_fwd(const uint16_t* q_nope, const uint16_t* q
                                        void* cuda_stream);
 
 /*
+ * Decode over the latent cache.  The MLA init excerpt on "Kimi K2 · Similarities" (section
+ * "Scale scores") has kv_a_proj_with_mqa produce a 512-wide latent row plus the shared
+ * 64-wide rotary key per token, and kv_b_proj map the latent to 64 heads x (128 no-rope
+ * key + 128 value).  A cache of latent rows holds 1152 bytes per token instead of the
+ * 32,896 of per-head keys and values.  This call computes, for Tq = 1 (query at the last
+ * position, causality vacuous) and every head h,
+ *
+ *   k_nope[b,h,j] = W[256h : 256h+128] . c_kv[b,j]      (no-rope key of key j)
+ *   v[b,h,j]      = W[256h+128 : 256h+256] . c_kv[b,j]  (value of key j)
+ *   out[b,h]      = the attention core of mla_attn_fwd on [q_nope | q_pe] and
+ *                   [k_nope | k_pe], keys j < kv_len[b]
+ *
+ * without materialising k_nope or v: the no-rope key rows of W are folded into the query
+ * (q_lat = W_K^T q_nope), the value rows applied once to the weighted latent sum.  Reading
+ * of the weight layout: per head, the first 128 of its 256 kv_b_proj output rows are the
+ * no-rope key, the next 128 the value.
+ *
+ *   q_nope [B, H, 128], q_pe [B, H, 64]           (bf16, device)
+ *   c_kv   [B, Tk, 512], k_pe [B, Tk, 64]         (bf16, device: the latent cache)
+ *   w_kvb  [H * 256, 512]                         (bf16, device: the kv_b_proj weight)
+ *   kv_len [B] int32 or NULL, out [B, H, 128]
+ * H must be at most 64.  Workspace: mla_latent_workspace_bytes(B, H, Tk), zeroed once.
+ * Errors as for mla_attn_fwd.
+ */
+MLA_API size_t mla_latent_workspace_bytes(int B, int H, int Tk);
+MLA_API mla_status mla_latent_decode_fwd(const uint16_t* q_nope, const uint16_t* q_pe,
+                                         const uint16_t* c_kv, const uint16_t* k_pe,
+                                         const uint16_t* w_kvb, const int32_t* kv_len, int B,
+                                         int H, int Tk, float softmax_scale, uint16_t* out,
+                                         void* workspace, size_t workspace_bytes,
+                                         void* cuda_stream);
+
+/*
  * Rotary embedding.  The attention excerpt on "Kimi K2 · Similarities" rotates the query's
  * and the new keys' rotary parts before the cache update (rotary_emb gives cos and sin for
  * the positions, apply_rotary_pos_emb rotates q_pe and k_pe), and the rope_scaling block of

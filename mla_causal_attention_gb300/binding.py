@@ -65,7 +65,8 @@ EXPORTED = ("mla_attn_workspace_bytes", "mla_attn_fwd", "mla_attn_fwd_ex",
             "mla_attn_get_status", "mla_status_string", "mla_attn_decode_plan",
             "mla_attn_append_fwd", "mla_rope_frequencies", "mla_rope_table",
             "mla_attn_rope_workspace_bytes", "mla_attn_rope_append_fwd",
-            "mla_attn_masked_workspace_bytes", "mla_attn_masked_fwd")
+            "mla_attn_masked_workspace_bytes", "mla_attn_masked_fwd",
+            "mla_latent_workspace_bytes", "mla_latent_decode_fwd")
 
 
 def library():
@@ -100,6 +101,10 @@ def library():
         lib.mla_attn_masked_workspace_bytes.argtypes = [i, i, i, i]
         lib.mla_attn_masked_fwd.restype = i
         lib.mla_attn_masked_fwd.argtypes = [p, p, p, p, p, p, p, i, i, i, i, i, f, p, p, sz, p]
+        lib.mla_latent_workspace_bytes.restype = sz
+        lib.mla_latent_workspace_bytes.argtypes = [i, i, i]
+        lib.mla_latent_decode_fwd.restype = i
+        lib.mla_latent_decode_fwd.argtypes = [p, p, p, p, p, p, i, i, i, f, p, p, sz, p]
         lib.mla_rope_frequencies.restype = i
         lib.mla_rope_frequencies.argtypes = [ctypes.POINTER(RopeConfig),
                                              ctypes.POINTER(ctypes.c_double),
@@ -309,6 +314,40 @@ def mla_attn_masked_fwd(q_nope, q_pe, k_nope, k_pe_shared, v, kv_len, key_mask,
                                      ws.numel(), ctypes.c_void_p(s.cuda_stream))
     if rc != 0:
         raise MlaAttnError(rc, "mla_attn_masked_fwd: ")
+    return out
+
+
+def mla_latent_decode_fwd(q_nope, q_pe, c_kv, k_pe, w_kvb, kv_len, softmax_scale: float,
+                          out=None, workspace: "Workspace | None" = None, stream=None):
+    """Decode over the latent cache: q_nope [B,H,128], q_pe [B,H,64], c_kv [B,Tk,512],
+    k_pe [B,Tk,64], w_kvb [H*256,512] (kv_b_proj weight), kv_len [B] int32 or None;
+    returns out [B,H,128]."""
+    lib = library()
+    dev = q_nope.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    B, H = q_nope.shape[:2]
+    Tk = c_kv.shape[1]
+    bf = torch.bfloat16
+    _check(q_nope, "q_nope", bf, (B, H, 128), dev)
+    _check(q_pe, "q_pe", bf, (B, H, 64), dev)
+    _check(c_kv, "c_kv", bf, (B, Tk, 512), dev)
+    _check(k_pe, "k_pe", bf, (B, Tk, 64), dev)
+    _check(w_kvb, "w_kvb", bf, (H * 256, 512), dev)
+    if kv_len is not None:
+        _check(kv_len, "kv_len", torch.int32, (B,), dev)
+    if out is None:
+        out = torch.empty((B, H, 128), dtype=bf, device=dev)
+    _check(out, "out", bf, (B, H, 128), dev)
+    ws = (workspace or _default_workspace(dev)).get(lib.mla_latent_workspace_bytes(B, H, Tk))
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        rc = lib.mla_latent_decode_fwd(_ptr(q_nope), _ptr(q_pe), _ptr(c_kv), _ptr(k_pe),
+                                       _ptr(w_kvb), _ptr(kv_len), B, H, Tk,
+                                       float(softmax_scale), _ptr(out), _ptr(ws), ws.numel(),
+                                       ctypes.c_void_p(s.cuda_stream))
+    if rc != 0:
+        raise MlaAttnError(rc, "mla_latent_decode_fwd: ")
     return out
 
 

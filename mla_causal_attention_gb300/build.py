@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmla_attn.so")
-SOURCES = ["host.cu", "decode.cu", "prefill.cu", "noalloc.cu", "rope.cu", "mask.cu"]
+SOURCES = ["host.cu", "decode.cu", "prefill.cu", "noalloc.cu", "rope.cu", "mask.cu", "latent.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

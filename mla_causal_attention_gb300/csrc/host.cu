@@ -73,6 +73,34 @@ size_t key_bits_bytes(int B, int Tk) {
   return ((size_t)B * ((Tk + 127) / 128) * 16 + 255) & ~(size_t)255;
 }
 
+// Latent-cache decode: keys per split in whole 128-key tiles.  One CTA per SM runs at a
+// time (its shared memory), and sequences of a ragged batch differ in length, so splits
+// are short enough (8 tiles) that the hardware scheduler balances a few waves of them;
+// a batch too small to fill the SMs splits further, down to one tile per split.  Each split
+// writes 64 heads x 512 fp32 partials, about 11% of an 8-tile split's input bytes.
+struct LatentPlan {
+  int chunk, splits;
+};
+LatentPlan plan_latent(int B, int Tk, int sms) {
+  const int tiles = (Tk + kLatTile - 1) / kLatTile;
+  int per = std::min(tiles, 8);
+  while (per > 1 && (int64_t)B * ((tiles + per - 1) / per) < sms) per = (per + 1) / 2;
+  LatentPlan pl;
+  pl.chunk = per * kLatTile;
+  pl.splits = (Tk + pl.chunk - 1) / pl.chunk;
+  return pl;
+}
+size_t r256(size_t x) { return (x + 255) & ~(size_t)255; }
+size_t latent_q_bytes(int B, int H) { return r256((size_t)B * H * 512 * 2); }
+size_t latent_ml_bytes(int B, int H, int splits) { return r256((size_t)B * H * splits * 8); }
+size_t latent_acc_bytes(int B, int H, int splits) {
+  return r256((size_t)B * H * splits * 512 * 4);
+}
+size_t latent_workspace(int B, int H, int splits) {
+  return kStatusBytes + latent_q_bytes(B, H) + latent_ml_bytes(B, H, splits) +
+         latent_acc_bytes(B, H, splits) + r256((size_t)B * H * 512 * 4);
+}
+
 // Rotary workspace: rotated queries [B,H,Tq,64] then rotated new rotary keys [B,Tq,64],
 // each on a 256-byte boundary, after the attention call's own workspace.
 size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -436,6 +464,51 @@ mla_status mla_attn_masked_fwd(const uint16_t* q_nope, const uint16_t* q_pe,
   return attention_impl(q_nope, q_pe, k_nope, k_pe_shared, v, kv_len, B, H, Tq, Tk, past_len,
                         softmax_scale, out, workspace, workspace_bytes, cuda_stream, nullptr, Tk,
                         nullptr, false, key_mask);
+}
+
+size_t mla_latent_workspace_bytes(int B, int H, int Tk) {
+  if (B < 1 || H < 1 || H > 64 || Tk < 1) return 0;
+  int sms = 0;
+  if (check_device(&sms) != MLA_OK || sms <= 0) sms = 152;
+  return latent_workspace(B, H, plan_latent(B, Tk, sms).splits);
+}
+
+mla_status mla_latent_decode_fwd(const uint16_t* q_nope, const uint16_t* q_pe,
+                                 const uint16_t* c_kv, const uint16_t* k_pe,
+                                 const uint16_t* w_kvb, const int32_t* kv_len, int B, int H,
+                                 int Tk, float softmax_scale, uint16_t* out, void* workspace,
+                                 size_t workspace_bytes, void* cuda_stream) {
+  if (!q_nope || !q_pe || !c_kv || !k_pe || !w_kvb || !out) return MLA_ERR_NULL;
+  if (!workspace) return MLA_ERR_WORKSPACE;
+  if (B < 1 || H < 1 || H > 64 || Tk < 1 || B > 65535) return MLA_ERR_SHAPE;
+  if ((int64_t)B * Tk * 512 > kMaxElems) return MLA_ERR_SHAPE;
+  if (!aligned16(q_nope) || !aligned16(q_pe) || !aligned16(c_kv) || !aligned16(k_pe) ||
+      !aligned16(w_kvb) || !aligned16(out) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(kv_len) & 3u) != 0)
+    return MLA_ERR_ALIGN;
+  if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.0f)) return MLA_ERR_ARG;
+  int sms = 0;
+  mla_status st = check_device(&sms);
+  if (st != MLA_OK) return st;
+  const LatentPlan pl = plan_latent(B, Tk, sms);
+  if (workspace_bytes < latent_workspace(B, H, pl.splits)) return MLA_ERR_WORKSPACE;
+  uint8_t* w = static_cast<uint8_t*>(workspace);
+  LatentArgs a{};
+  a.q_nope = q_nope; a.q_pe = q_pe; a.c_kv = c_kv; a.k_pe = k_pe; a.w_kvb = w_kvb;
+  a.kv_len = kv_len; a.out = out;
+  a.status = reinterpret_cast<int*>(w);
+  uint8_t* cur = w + kStatusBytes;
+  a.q_lat = reinterpret_cast<uint16_t*>(cur);
+  cur += latent_q_bytes(B, H);
+  a.part_ml = reinterpret_cast<float*>(cur);
+  cur += latent_ml_bytes(B, H, pl.splits);
+  a.part_acc = reinterpret_cast<float*>(cur);
+  cur += latent_acc_bytes(B, H, pl.splits);
+  a.o_lat = reinterpret_cast<float*>(cur);
+  a.B = B; a.H = H; a.Tk = Tk; a.kv_rows = Tk; a.chunk = pl.chunk; a.splits = pl.splits;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  return launch_latent(a, static_cast<cudaStream_t>(cuda_stream)) == cudaSuccess ? MLA_OK
+                                                                                  : MLA_ERR_CUDA;
 }
 
 mla_status mla_attn_fwd(const uint16_t* q_nope, const uint16_t* q_pe, const uint16_t* k_nope,

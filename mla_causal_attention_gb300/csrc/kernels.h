@@ -2,6 +2,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "mla_attn.h"
@@ -133,6 +134,34 @@ struct FixupArgs {
   int B, H, Tq, Tk, past_len, kv_rows;
 };
 cudaError_t launch_masked_rows_fixup(const FixupArgs& a, cudaStream_t stream);
+
+// bf16 tensor viewed as {inner, rows, planes} (planes plane_rows rows apart) as a tensor
+// map with 128-byte swizzled {64, box_rows, 1} boxes; rows past `rows` read as zeros.
+bool encode_bf16_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+                    uint64_t planes, uint64_t plane_rows, uint32_t box_rows);
+
+// Decode over the latent cache (absorbed kv_b_proj).  Shapes: q_nope [B,H,128], q_pe
+// [B,H,64], c_kv [B,kv_rows,512], k_pe [B,kv_rows,64], w_kvb [H*256,512]; out [B,H,128].
+// Workspace pieces (device): q_lat bf16 [B,H,512], part_ml f32 [B*H*splits][2], part_acc
+// f32 [B*H*splits][512], o_lat f32 [B,H,512].
+struct LatentArgs {
+  const uint16_t* q_nope;
+  const uint16_t* q_pe;
+  const uint16_t* c_kv;
+  const uint16_t* k_pe;
+  const uint16_t* w_kvb;
+  const int32_t* kv_len;
+  uint16_t* out;
+  uint16_t* q_lat;
+  float* part_ml;
+  float* part_acc;
+  float* o_lat;
+  int* status;
+  int B, H, Tk, kv_rows, chunk, splits;
+  float scale_log2;
+};
+constexpr int kLatTile = 128;  // keys per tile of the latent kernel
+cudaError_t launch_latent(const LatentArgs& a, cudaStream_t stream);
 
 // Number of SMs of the current device (cached per device).
 int device_sm_count();

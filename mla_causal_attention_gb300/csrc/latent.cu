@@ -1,0 +1,741 @@
+// latent.cu -- decode over MLA's latent cache with the key/value up-projection absorbed,
+// on sm_103a tensor cores.
+//
+// The MLA init excerpt on "Kimi K2 · Similarities" (§Scale scores) gives the joint key/value
+// down-projection (kv_a_proj_with_mqa: a 512-wide latent plus the shared 64-wide rotary key)
+// and the up-projection kv_b_proj: 512 -> 64 heads x (128 no-rope key + 128 value).  The
+// cache can therefore hold the latent row c_j (and the rotary key) instead of 64 heads'
+// keys and values, 1152 bytes per token instead of 32,896.  With W_K[h], W_V[h] the
+// 128 x 512 blocks of kv_b_proj for head h:
+//   q_nope . k_nope_j = q_nope . (W_K c_j) = (W_K^T q_nope) . c_j = q_lat . c_j
+//   sum_j p_j v_j     = sum_j p_j W_V c_j  = W_V (sum_j p_j c_j)   = W_V o_lat
+// so the attention runs over the latent rows for all 64 heads at once (one shared "key"
+// [c_j | k_pe_j] of 576 columns, one shared "value" c_j of 512), between two small per-head
+// projections.
+//
+// Kernels:
+//   latent_absorb_kernel   q_lat[b,h] = W_K[h]^T q_nope[b,h]                 (bf16 out)
+//   latent_splitkv_kernel  per (sequence, key split): scores of 128-key tiles for the 64
+//                          heads, online softmax per head, o_lat partials
+//   latent_combine_kernel  merges the splits' (max, sum, o_lat) per (sequence, head)
+//   latent_upproj_kernel   out[b,h] = W_V[h] o_lat[b,h]                     (bf16 out)
+//
+// The split kernel runs both MMAs transposed, with keys (and latent columns) on the
+// 128 TMEM lanes and the 64 heads as the N dimension:
+//   S^T[128 keys, 64 heads]   = K_tile[128, 576] . Q^T        A = K tile (K-major), B = Q
+//   O^T[512, 64 heads]       += C_tile^T[512, 128] . P^T      4 M-blocks of 128 latent
+//                                                             columns; A = the tile's
+//                                                             latent rows read MN-major,
+//                                                             B = P^T from shared memory
+// so O^T takes 4 x 64 TMEM columns (a head-major O would need all 512).  The tile's eight
+// 64-column latent sub-tiles stay in eight fixed slots from the score pass through the
+// value pass (latent sub-tile s of every tile lives in slot s); its rotary-key sub-tile is
+// loaded into the P^T buffer, which is free during the score pass.  Each value block
+// releases its two slots, so the next tile's first sub-tiles load while the current value
+// mixes still run.
+#include <cuda.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "tcgen05.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kLD = 512;          // latent width (kv_lora_rank)
+constexpr int kLSubK = 16384;     // 128 keys x 64 columns, bf16, 128-byte swizzled
+constexpr int kLSubQ = 8192;      // 64 heads x 64 columns
+constexpr int kLSlots = 8;        // latent sub-tile s of every key tile lives in slot s
+constexpr int kLThreads = 256;    // warp 0 producer, warp 1 MMA, warps 4-7 softmax
+constexpr int kLOffQ = 0;                             // 9 sub-tiles: q_lat 0-511, q_pe
+constexpr int kLOffRing = kLOffQ + 9 * kLSubQ;        // 73728
+constexpr int kLOffP = kLOffRing + kLSlots * kLSubK;  // 204800: the tile's rotary keys
+                                                      // (16 KB), then P^T (2 sub-tiles)
+constexpr int kLOffRed = kLOffP + kLSubK;             // 221184: softmax scratch
+constexpr int kLOffBar = kLOffRed + 4096;             // 225280
+constexpr int kLSmem = kLOffBar + 256 + 1024;         // + barriers + alignment slack
+static_assert(kLSmem <= 232448, "shared memory per block");
+constexpr float kLRescale = 8.0f;  // log2 units, as in the prefill kernel
+
+struct LatentParams {
+  CUtensorMap tm_q;   // q_lat {512, H, B}, boxes {64, 64, 1}
+  CUtensorMap tm_qr;  // q_pe  {64, H, B},  boxes {64, 64, 1}
+  CUtensorMap tm_c;   // c_kv  {512, Tk, B}, boxes {64, 128, 1}
+  CUtensorMap tm_kr;  // k_pe  {64, Tk, B},  boxes {64, 128, 1}
+  const int32_t* kv_len;
+  float* part_ml;
+  float* part_acc;
+  int* status;
+  int B, H, Tk, chunk, splits;
+  float scale_log2;
+};
+
+struct LBars {
+  uint64_t full[kLSlots];   // slot s holds the current tile's latent sub-tile s
+  uint64_t empty[kLSlots];  // slot s released by the value block that read it
+  uint64_t pe_full;         // the tile's rotary keys are in the P^T buffer
+  uint64_t pe_free;         // the previous tile's value mixes are done with P^T
+  uint64_t q_full;
+  uint64_t s_full;          // S^T of the tile in TMEM
+  uint64_t p_ready;         // P^T in shared memory, O^T rescaled (4 warp arrivals)
+  uint64_t o_done;          // last value mix done
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+static_assert(sizeof(LBars) <= 256, "barrier block");
+
+__device__ __forceinline__ void ldrain(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(a, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return;
+  }
+}
+
+// Barrier over the 4 softmax warps (named barrier 1) that ANDs a predicate across them.
+__device__ __forceinline__ bool softmax_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n"
+      " bar.red.and.pred po, 1, 128, pi;\n selp.u32 %0, 1, 0, po;\n}"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void softmax_sync() {
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+struct OpMax {
+  __device__ __forceinline__ float operator()(float a, float b) const { return fmaxf(a, b); }
+};
+struct OpAdd {
+  __device__ __forceinline__ float operator()(float a, float b) const { return a + b; }
+};
+
+// Reduces 64 per-head values over the 32 lanes of a warp by halving exchanges (31 x 2
+// shuffles instead of 64 x 5): lane l ends with the results for heads 2l and 2l + 1.
+template <class Op>
+__device__ __forceinline__ void halving_reduce64(const float (&v)[64], float (&out)[2],
+                                                 int lane, Op op) {
+  float a[32], c[16], d[8], e[4];
+  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2, b0 = lane & 1;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float keep = b4 ? v[i + 32] : v[i], send = b4 ? v[i] : v[i + 32];
+    a[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+  }
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float keep = b3 ? a[i + 16] : a[i], send = b3 ? a[i] : a[i + 16];
+    c[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float keep = b2 ? c[i + 8] : c[i], send = b2 ? c[i] : c[i + 8];
+    d[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float keep = b1 ? d[i + 4] : d[i], send = b1 ? d[i] : d[i + 4];
+    e[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 2));
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float keep = b0 ? e[i + 2] : e[i], send = b0 ? e[i] : e[i + 2];
+    out[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 1));
+  }
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__global__ void __launch_bounds__(kLThreads, 1)
+    latent_splitkv_kernel(const __grid_constant__ LatentParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  uint8_t* sQ = smem + kLOffQ;
+  uint8_t* sRing = smem + kLOffRing;
+  uint8_t* sP = smem + kLOffP;
+  LBars* bars = reinterpret_cast<LBars*>(smem + kLOffBar);
+  volatile int* abort_flag = &bars->abort_flag;
+
+  const int split = blockIdx.x;
+  const int b = blockIdx.y;
+  int kvl = p.kv_len ? p.kv_len[b] : p.Tk;
+  if (kvl < 1 || kvl > p.Tk) {
+    if (threadIdx.x == 0 && split == 0) set_status(p.status, MLA_ERR_KVLEN);
+    kvl = min(max(kvl, 1), p.Tk);
+  }
+  const int j0 = split * p.chunk;
+  if (j0 >= kvl) return;  // uniform: this split holds no visible key (the combine skips it)
+  const int j1 = min(j0 + p.chunk, kvl);
+  const int nt = (j1 - j0 + kLatTile - 1) / kLatTile;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kLSlots; ++i) {
+      mbar_init(&bars->full[i], 1);
+      mbar_init(&bars->empty[i], 1);
+    }
+    mbar_init(&bars->pe_full, 1);
+    mbar_init(&bars->pe_free, 1);
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->s_full, 1);
+    mbar_init(&bars->p_ready, 4);
+    mbar_init(&bars->o_done, 1);
+    mbar_init(&bars->mma_done, 1);
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&bars->tmem_base, 512);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tbase = bars->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ================= TMA producer =================
+      prefetch_tmap(&p.tm_q);
+      prefetch_tmap(&p.tm_qr);
+      prefetch_tmap(&p.tm_c);
+      prefetch_tmap(&p.tm_kr);
+      mbar_arrive_expect_tx(&bars->q_full, 9 * kLSubQ);
+      for (int s = 0; s < 8; ++s)
+        tma_load_3d_nohint(sQ + s * kLSubQ, &p.tm_q, &bars->q_full, 64 * s, 0, b);
+      tma_load_3d_nohint(sQ + 8 * kLSubQ, &p.tm_qr, &bars->q_full, 0, 0, b);
+      bool ok = true;
+      int posted = 0;  // key tiles whose loads were issued
+      for (int j = 0; j < nt && ok; ++j) {
+        const int jt = j0 + j * kLatTile;
+        const uint32_t prev = (uint32_t)(j - 1) & 1u;
+        // Latent columns 0-511: sub-tile s into slot s once the previous tile's value block
+        // s / 2 has released it.
+        for (int sidx = 0; sidx < kLSlots; ++sidx) {
+          if (j > 0) ok = mbar_wait(&bars->empty[sidx], prev, p.status, abort_flag);
+          if (!ok) break;
+          mbar_arrive_expect_tx(&bars->full[sidx], kLSubK);
+          tma_load_3d_nohint(sRing + sidx * kLSubK, &p.tm_c, &bars->full[sidx], 64 * sidx, jt,
+                             b);
+        }
+        if (!ok) break;
+        // Rotary keys into the P^T buffer once the previous tile's value mixes are done.
+        if (j > 0) ok = mbar_wait(&bars->pe_free, prev, p.status, abort_flag);
+        if (!ok) break;
+        mbar_arrive_expect_tx(&bars->pe_full, kLSubK);
+        tma_load_3d_nohint(sP, &p.tm_kr, &bars->pe_full, 0, jt, b);
+        posted = j + 1;
+      }
+      // Every load issued must land before shared memory is released: each barrier has at
+      // most its last phase in flight.
+      ldrain(&bars->q_full, 0);
+      if (posted > 0) {
+        for (int sidx = 0; sidx < kLSlots; ++sidx)
+          ldrain(&bars->full[sidx], (uint32_t)(posted - 1) & 1u);
+        ldrain(&bars->pe_full, (uint32_t)(posted - 1) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    // ================= MMA issuer =================
+    constexpr uint32_t kIdQK = tc::idesc_bf16_f32_ab(128, 64, false, false);
+    constexpr uint32_t kIdPV = tc::idesc_bf16_f32_ab(128, 64, true, false);
+    const uint64_t dhi_k = tc::smem_desc_sw128(0, 16, 1024);
+    const uint64_t dhi_mn = tc::smem_desc_sw128(0, kLSubK, 1024);  // slots 2q, 2q+1 adjacent
+    const uint32_t q_lo = smem_u32(sQ) >> 4;
+    const uint32_t ring_lo = smem_u32(sRing) >> 4;
+    const uint32_t p_lo = smem_u32(sP) >> 4;
+    const uint32_t s_tmem = tbase;       // S^T: 64 columns
+    const uint32_t o_tmem = tbase + 64;  // O^T: 4 blocks of 64 columns
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_full, 0, p.status, abort_flag));
+    tc::fence_after_sync();
+    for (int j = 0; j < nt && ok; ++j) {
+      const uint32_t ph = (uint32_t)j & 1u;
+      // S^T = K_tile Q^T over 576 columns: 4 k-steps of 16 per 64-column sub-tile; the
+      // rotary-key sub-tile (in the P^T buffer) last.
+      for (int sidx = 0; sidx < 9; ++sidx) {
+        uint64_t* fb = sidx < 8 ? &bars->full[sidx] : &bars->pe_full;
+        ok = __all_sync(0xffffffffu, mbar_wait(fb, ph, p.status, abort_flag));
+        if (!ok) break;
+        tc::fence_after_sync();
+        const uint32_t a_lo = sidx < 8 ? ring_lo + sidx * (kLSubK >> 4) : p_lo;
+        if (tc::elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint32_t koff = kk * (32 >> 4);
+            const uint64_t adesc = dhi_k | (uint64_t)(a_lo + koff);
+            const uint64_t bdesc = dhi_k | (uint64_t)(q_lo + sidx * (kLSubQ >> 4) + koff);
+            tc::mma_ss(s_tmem, adesc, bdesc, kIdQK, (sidx | kk) != 0 ? 1u : 0u);
+          }
+          if (sidx == 8) tc::commit(&bars->s_full);
+        }
+        __syncwarp();
+      }
+      if (!ok) break;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->p_ready, ph, p.status, abort_flag));
+      if (!ok) break;
+      tc::fence_after_sync();
+      // O^T block q (latent columns 128q..128q+127) += C_tile^T P^T over the tile's keys:
+      // A = slots 2q and 2q + 1 read MN-major, B = P^T.
+      if (tc::elect_one()) {
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t adesc =
+                dhi_mn | (uint64_t)(ring_lo + 2 * q * (kLSubK >> 4) + kk * (2048 >> 4));
+            const uint64_t bdesc =
+                dhi_k | (uint64_t)(p_lo + (kk >> 2) * (kLSubQ >> 4) + (kk & 3) * (32 >> 4));
+            tc::mma_ss(o_tmem + 64 * q, adesc, bdesc, kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc::commit(&bars->empty[2 * q]);
+          tc::commit(&bars->empty[2 * q + 1]);
+        }
+        tc::commit(&bars->pe_free);
+      }
+      __syncwarp();
+    }
+    if (tc::elect_one()) {
+      if (ok) tc::commit(&bars->o_done);
+      tc::commit(&bars->mma_done);
+    }
+    __syncwarp();
+    ldrain(&bars->mma_done, 0);
+  } else if (warp >= 4) {
+    // ================= softmax warps =================
+    // Thread = key row r of the tile = TMEM lane r; its S^T row holds the 64 heads' scores.
+    const int sw = warp - 4;
+    const int r = sw * 32 + lane;
+    const int t = threadIdx.x - 128;  // owner of head t when t < 64
+    const uint32_t lane_off = (uint32_t)(sw * 32) << 16;
+    const uint32_t s_t = tbase + lane_off;
+    const uint32_t o_t = tbase + lane_off + 64;
+    float* red_max = reinterpret_cast<float*>(smem + kLOffRed);  // [4 warps][64 heads]
+    float* red_sum = red_max + 256;                               // [4][64]
+    float* mbase = red_sum + 256;                                 // [64] exponent base
+    float* alpha_s = mbase + 64;                                  // [64] this tile's rescale
+    int* any_rescale = reinterpret_cast<int*>(alpha_s + 64);      // [2], by tile parity
+    const float sl2 = p.scale_log2;
+    float m_own = -INFINITY, l_own = 0.f;  // running max (log2 units) and sum of head t
+    if (t < 2) any_rescale[t] = 0;
+    softmax_sync();
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      const bool got =
+          __all_sync(0xffffffffu, mbar_wait(&bars->s_full, j & 1, p.status, abort_flag));
+      float v[64];
+      if (got) {
+        tc::fence_after_sync();
+        uint32_t ra[32], rb[32];
+        tc::tmem_ld32(s_t, ra);
+        tc::tmem_ld32(s_t + 32, rb);
+        tc::tmem_wait_ld();
+        const bool vis = j0 + j * kLatTile + r < j1;
+#pragma unroll
+        for (int h = 0; h < 32; ++h) {
+          v[h] = vis ? __uint_as_float(ra[h]) : -INFINITY;
+          v[h + 32] = vis ? __uint_as_float(rb[h]) : -INFINITY;
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < 64; ++h) v[h] = -INFINITY;
+      }
+      float w2[2];
+      halving_reduce64(v, w2, lane, OpMax());
+      red_max[sw * 64 + 2 * lane] = w2[0];
+      red_max[sw * 64 + 2 * lane + 1] = w2[1];
+      if (!softmax_and(got)) {  // barrier A; every warp leaves together on a failed wait
+        ok = false;
+        break;
+      }
+      if (t < 64) {
+        const float tm = fmaxf(fmaxf(red_max[t], red_max[64 + t]),
+                               fmaxf(red_max[128 + t], red_max[192 + t])) * sl2;
+        float a = 1.f;
+        if (j == 0) {
+          m_own = tm;  // key j0 < kv_len is visible: finite
+        } else if (tm > m_own + kLRescale) {
+          a = ex2_approx(m_own - tm);
+          m_own = tm;
+          l_own *= a;
+        }
+        mbase[t] = m_own;
+        alpha_s[t] = a;
+        if (a != 1.f) any_rescale[j & 1] = 1;
+      } else if (t == 64) {
+        any_rescale[(j + 1) & 1] = 0;  // everyone read it before barrier A of this tile
+      }
+      softmax_sync();  // barrier B
+      float pv[64];
+#pragma unroll
+      for (int h = 0; h < 64; h += 4) {
+        const float4 mb = *reinterpret_cast<const float4*>(mbase + h);
+        pv[h] = ex2_approx(fmaf(v[h], sl2, -mb.x));
+        pv[h + 1] = ex2_approx(fmaf(v[h + 1], sl2, -mb.y));
+        pv[h + 2] = ex2_approx(fmaf(v[h + 2], sl2, -mb.z));
+        pv[h + 3] = ex2_approx(fmaf(v[h + 3], sl2, -mb.w));
+      }
+      if (any_rescale[j & 1]) {
+        // O^T columns of heads whose max grew: this thread's lane in each of the 4 blocks.
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+#pragma unroll
+          for (int hh = 0; hh < 64; hh += 32) {
+            uint32_t o[32];
+            tc::tmem_ld32(o_t + 64 * q + hh, o);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha_s[hh + e]);
+            tc::tmem_st32(o_t + 64 * q + hh, o);
+          }
+        }
+        tc::tmem_wait_st();
+      }
+      float s2[2];
+      halving_reduce64(pv, s2, lane, OpAdd());
+      red_sum[sw * 64 + 2 * lane] = s2[0];
+      red_sum[sw * 64 + 2 * lane + 1] = s2[1];
+      // P^T [64 heads x 128 keys] bf16, 128-byte swizzled like a TMA tile: keys r and r ^ 1
+      // are lanes l and l ^ 1, so even lanes store heads 0-31 and odd lanes heads 32-63,
+      // each word holding the pair (key r & ~1, key r | 1).
+      {
+        const bool odd = lane & 1;
+        const int kp = r & ~1;
+        uint8_t* pb = sP + (kp >> 6) * kLSubQ;
+        const int kin = kp & 63;
+        const int chunk = (kin * 2) >> 4, within = (kin * 2) & 15;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float mine = odd ? pv[i + 32] : pv[i];
+          const float send = odd ? pv[i] : pv[i + 32];
+          const float other = __shfl_xor_sync(0xffffffffu, send, 1);
+          const int h = odd ? i + 32 : i;
+          const uint32_t word = odd ? pack_bf16x2(other, mine) : pack_bf16x2(mine, other);
+          *reinterpret_cast<uint32_t*>(pb + (h >> 3) * 1024 + (h & 7) * 128 +
+                                       ((chunk ^ (h & 7)) << 4) + within) = word;
+        }
+      }
+      fence_proxy_async_smem();  // P^T written by threads, read by the tensor core
+      tc::fence_before_sync();
+      softmax_sync();  // barrier C
+      if (t < 64) l_own += (red_sum[t] + red_sum[64 + t]) + (red_sum[128 + t] + red_sum[192 + t]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->p_ready);
+    }
+    if (ok) {
+      if (__all_sync(0xffffffffu, mbar_wait(&bars->o_done, 0, p.status, abort_flag))) {
+        tc::fence_after_sync();
+        const size_t row0 = (size_t)b * p.H * p.splits + split;  // (b, head 0, split)
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+          uint32_t oa[32], ob[32];
+          tc::tmem_ld32(o_t + 64 * q, oa);
+          tc::tmem_ld32(o_t + 64 * q + 32, ob);
+          tc::tmem_wait_ld();
+          const int d = 128 * q + r;
+#pragma unroll
+          for (int h = 0; h < 64; ++h) {
+            if (h < p.H)
+              p.part_acc[(row0 + (size_t)h * p.splits) * kLD + d] =
+                  __uint_as_float(h < 32 ? oa[h] : ob[h - 32]);
+          }
+        }
+        if (t < p.H)
+          *reinterpret_cast<float2*>(p.part_ml + (row0 + (size_t)t * p.splits) * 2) =
+              make_float2(m_own, l_own);
+      }
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tbase, 512);
+  }
+}
+
+// Warp-level bf16 MMA (m16n8k16, fp32 accumulate) for the two per-head projections: small
+// GEMMs (16 sequences x 128 or 512 columns x 512 or 128) whose operands sit in shared
+// memory.  Fragments (g = lane / 4, c = lane % 4): A a0 (row g, cols 2c, 2c+1), a1 (row
+// g+8), a2 (cols + 8), a3 (row g+8, cols + 8); B b0 (rows k = 2c, 2c+1, col g), b1 (k + 8);
+// C c0, c1 (row g, cols 2c, 2c+1), c2, c3 (row g+8).
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+constexpr int kWRow = kLD + 8;    // padded shared-memory row of W (bf16): conflict-free
+constexpr int kQRow = 128 + 8;    // padded row of 128 bf16
+constexpr int kAbsorbSmem = 128 * kWRow * 2 + 16 * kQRow * 2;
+constexpr int kUpSmem = 128 * kWRow * 2 + 16 * kWRow * 2;
+
+// Copies rows [row0, row0 + 128) of w_kvb (512 bf16 each) into padded shared memory with
+// asynchronous 16-byte copies (all in flight at once); the caller waits with
+// cp_async_wait_all and a block barrier.
+__device__ __forceinline__ void stage_w(uint16_t* sw, const uint16_t* w_kvb, size_t row0) {
+  const uint4* src = reinterpret_cast<const uint4*>(w_kvb + row0 * kLD);
+  for (int i = threadIdx.x; i < 128 * (kLD / 8); i += blockDim.x) {
+    const int r = i / (kLD / 8), c = i % (kLD / 8);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                     smem_u32(sw + r * kWRow + c * 8)),
+                 "l"(src + i)
+                 : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// q_lat[b,h,:] = W_K[h]^T q_nope[b,h]: per (head, 16 sequences) a [16 x 128] . [128 x 512]
+// GEMM; warp w computes latent columns [64w, 64w + 64).
+__global__ void __launch_bounds__(256) latent_absorb_kernel(const LatentArgs a) {
+  extern __shared__ __align__(16) uint8_t ab_smem[];
+  uint16_t* sw = reinterpret_cast<uint16_t*>(ab_smem);  // W_K[h]: 128 rows (k) x 512 (n)
+  uint16_t* sq = sw + 128 * kWRow;                       // q_nope: 16 rows (m) x 128 (k)
+  const int h = blockIdx.x;
+  const int b0 = blockIdx.y * 16;
+  const int nb = min(16, a.B - b0);
+  stage_w(sw, a.w_kvb, (size_t)h * 256);
+  for (int i = threadIdx.x; i < 16 * 16; i += blockDim.x) {
+    const int r = i >> 4, c = i & 15;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (r < nb) v = reinterpret_cast<const uint4*>(a.q_nope + ((size_t)(b0 + r) * a.H + h) * 128)[c];
+    *reinterpret_cast<uint4*>(sq + r * kQRow + c * 8) = v;
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c2 = (lane & 3) * 2;
+  float acc[8][4];
+#pragma unroll
+  for (int n = 0; n < 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+#pragma unroll
+  for (int k0 = 0; k0 < 128; k0 += 16) {
+    uint32_t af[4];
+    af[0] = *reinterpret_cast<const uint32_t*>(sq + g * kQRow + k0 + c2);
+    af[1] = *reinterpret_cast<const uint32_t*>(sq + (g + 8) * kQRow + k0 + c2);
+    af[2] = *reinterpret_cast<const uint32_t*>(sq + g * kQRow + k0 + c2 + 8);
+    af[3] = *reinterpret_cast<const uint32_t*>(sq + (g + 8) * kQRow + k0 + c2 + 8);
+#pragma unroll
+    for (int n = 0; n < 8; ++n) {
+      const int col = warp * 64 + n * 8 + g;  // B[k][n] = W_K[k][col]: rows k, k + 1
+      const uint16_t* wk = sw + (k0 + c2) * kWRow + col;
+      const uint32_t b0 = (uint32_t)wk[0] | ((uint32_t)wk[kWRow] << 16);
+      const uint32_t b1 = (uint32_t)wk[8 * kWRow] | ((uint32_t)wk[9 * kWRow] << 16);
+      mma16816(acc[n], af, b0, b1);
+    }
+  }
+#pragma unroll
+  for (int n = 0; n < 8; ++n) {
+    const int col = warp * 64 + n * 8 + c2;
+    if (g < nb)
+      *reinterpret_cast<uint32_t*>(a.q_lat + ((size_t)(b0 + g) * a.H + h) * kLD + col) =
+          pack_bf16x2(acc[n][0], acc[n][1]);
+    if (g + 8 < nb)
+      *reinterpret_cast<uint32_t*>(a.q_lat + ((size_t)(b0 + g + 8) * a.H + h) * kLD + col) =
+          pack_bf16x2(acc[n][2], acc[n][3]);
+  }
+}
+
+// One warp per (b, h): o_lat = sum_s 2^(m_s - m) acc_s / sum_s 2^(m_s - m) l_s over the
+// splits that hold visible keys; lane owns columns 4 lane + 128 k, k = 0..3.
+__global__ void __launch_bounds__(256) latent_combine_kernel(const LatentArgs a) {
+  const int w = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (w >= a.B * a.H) return;
+  const int b = w / a.H;
+  int kvl = a.kv_len ? a.kv_len[b] : a.Tk;
+  kvl = min(max(kvl, 1), a.Tk);
+  const int n = (kvl + a.chunk - 1) / a.chunk;
+  const size_t base = (size_t)w * a.splits;
+  float m = -INFINITY;
+  for (int s = lane; s < n; s += 32) m = fmaxf(m, a.part_ml[(base + s) * 2]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float l = 0.f;
+  float4 acc[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < n; ++s) {
+    const float2 ml = *reinterpret_cast<const float2*>(a.part_ml + (base + s) * 2);
+    const float f = ex2_approx(ml.x - m);
+    l += f * ml.y;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float4 v =
+          *reinterpret_cast<const float4*>(a.part_acc + (base + s) * kLD + 128 * k + 4 * lane);
+      acc[k].x = fmaf(f, v.x, acc[k].x);
+      acc[k].y = fmaf(f, v.y, acc[k].y);
+      acc[k].z = fmaf(f, v.z, acc[k].z);
+      acc[k].w = fmaf(f, v.w, acc[k].w);
+    }
+  }
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float4 o = acc[k];
+    o.x *= inv;
+    o.y *= inv;
+    o.z *= inv;
+    o.w *= inv;
+    *reinterpret_cast<float4*>(a.o_lat + (size_t)w * kLD + 128 * k + 4 * lane) = o;
+  }
+}
+
+// out[b,h,:] = W_V[h] o_lat[b,h]: per (head, 16 sequences) a [16 x 512] . [512 x 128] GEMM
+// (o_lat rounded to bf16 as the MMA operand); warp w computes output columns [16w, 16w+16).
+__global__ void __launch_bounds__(256) latent_upproj_kernel(const LatentArgs a) {
+  extern __shared__ __align__(16) uint8_t up_smem[];
+  uint16_t* sw = reinterpret_cast<uint16_t*>(up_smem);  // W_V[h]: 128 rows (n) x 512 (k)
+  uint16_t* so = sw + 128 * kWRow;                       // o_lat: 16 rows (m) x 512 (k)
+  const int h = blockIdx.x;
+  const int b0 = blockIdx.y * 16;
+  const int nb = min(16, a.B - b0);
+  stage_w(sw, a.w_kvb, (size_t)h * 256 + 128);
+  for (int i = threadIdx.x; i < 16 * (kLD / 4); i += blockDim.x) {
+    const int r = i / (kLD / 4), c = i % (kLD / 4);
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (r < nb) v = reinterpret_cast<const float4*>(a.o_lat + ((size_t)(b0 + r) * a.H + h) * kLD)[c];
+    *reinterpret_cast<uint2*>(so + r * kWRow + c * 4) =
+        make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c2 = (lane & 3) * 2;
+  float acc[2][4];
+#pragma unroll
+  for (int n = 0; n < 2; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+#pragma unroll 4
+  for (int k0 = 0; k0 < kLD; k0 += 16) {
+    uint32_t af[4];
+    af[0] = *reinterpret_cast<const uint32_t*>(so + g * kWRow + k0 + c2);
+    af[1] = *reinterpret_cast<const uint32_t*>(so + (g + 8) * kWRow + k0 + c2);
+    af[2] = *reinterpret_cast<const uint32_t*>(so + g * kWRow + k0 + c2 + 8);
+    af[3] = *reinterpret_cast<const uint32_t*>(so + (g + 8) * kWRow + k0 + c2 + 8);
+#pragma unroll
+    for (int n = 0; n < 2; ++n) {
+      const uint16_t* wr = sw + (warp * 16 + n * 8 + g) * kWRow + k0 + c2;  // B[k][n] = W_V[n][k]
+      mma16816(acc[n], af, *reinterpret_cast<const uint32_t*>(wr),
+               *reinterpret_cast<const uint32_t*>(wr + 8));
+    }
+  }
+#pragma unroll
+  for (int n = 0; n < 2; ++n) {
+    const int col = warp * 16 + n * 8 + c2;
+    if (g < nb)
+      *reinterpret_cast<uint32_t*>(a.out + ((size_t)(b0 + g) * a.H + h) * 128 + col) =
+          pack_bf16x2(acc[n][0], acc[n][1]);
+    if (g + 8 < nb)
+      *reinterpret_cast<uint32_t*>(a.out + ((size_t)(b0 + g + 8) * a.H + h) * 128 + col) =
+          pack_bf16x2(acc[n][2], acc[n][3]);
+  }
+}
+
+// Tensor maps, cached by pointers and sizes (encoding costs microseconds of host time).
+struct LMapKey {
+  const void* ptr[4];
+  int B, H, Tk, kv_rows;
+  bool operator==(const LMapKey& o) const {
+    for (int i = 0; i < 4; ++i)
+      if (ptr[i] != o.ptr[i]) return false;
+    return B == o.B && H == o.H && Tk == o.Tk && kv_rows == o.kv_rows;
+  }
+};
+struct LMapEntry {
+  LMapKey key;
+  CUtensorMap maps[4];
+  bool valid;
+};
+std::mutex g_lmap_mu;
+LMapEntry g_lmap[8];
+int g_lmap_next = 0;
+
+bool latent_maps(const LatentArgs& a, LatentParams* p) {
+  const LMapKey key = {{a.q_lat, a.q_pe, a.c_kv, a.k_pe}, a.B, a.H, a.Tk, a.kv_rows};
+  std::lock_guard<std::mutex> lk(g_lmap_mu);
+  for (const LMapEntry& e : g_lmap) {
+    if (e.valid && e.key == key) {
+      p->tm_q = e.maps[0];
+      p->tm_qr = e.maps[1];
+      p->tm_c = e.maps[2];
+      p->tm_kr = e.maps[3];
+      return true;
+    }
+  }
+  if (!encode_bf16_3d(&p->tm_q, a.q_lat, kLD, a.H, a.B, a.H, 64) ||
+      !encode_bf16_3d(&p->tm_qr, a.q_pe, 64, a.H, a.B, a.H, 64) ||
+      !encode_bf16_3d(&p->tm_c, a.c_kv, kLD, a.Tk, a.B, a.kv_rows, 128) ||
+      !encode_bf16_3d(&p->tm_kr, a.k_pe, 64, a.Tk, a.B, a.kv_rows, 128))
+    return false;
+  LMapEntry& e = g_lmap[g_lmap_next];
+  g_lmap_next = (g_lmap_next + 1) % 8;
+  e.key = key;
+  e.maps[0] = p->tm_q;
+  e.maps[1] = p->tm_qr;
+  e.maps[2] = p->tm_c;
+  e.maps[3] = p->tm_kr;
+  e.valid = true;
+  return true;
+}
+
+}  // namespace
+
+cudaError_t launch_latent(const LatentArgs& a, cudaStream_t stream) {
+  LatentParams p;
+  if (!latent_maps(a, &p)) return cudaErrorInvalidValue;
+  p.kv_len = a.kv_len;
+  p.part_ml = a.part_ml;
+  p.part_acc = a.part_acc;
+  p.status = a.status;
+  p.B = a.B;
+  p.H = a.H;
+  p.Tk = a.Tk;
+  p.chunk = a.chunk;
+  p.splits = a.splits;
+  p.scale_log2 = a.scale_log2;
+
+  static int attr_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (attr_device != dev) {
+    e = cudaFuncSetAttribute(latent_splitkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kLSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(latent_upproj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kUpSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(latent_absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kAbsorbSmem);
+    if (e != cudaSuccess) return e;
+    attr_device = dev;
+  }
+  const unsigned bgroups = (unsigned)((a.B + 15) / 16);
+  latent_absorb_kernel<<<dim3(a.H, bgroups), 256, kAbsorbSmem, stream>>>(a);
+  latent_splitkv_kernel<<<dim3(a.splits, a.B), kLThreads, kLSmem, stream>>>(p);
+  latent_combine_kernel<<<(unsigned)((a.B * a.H + 7) / 8), 256, 0, stream>>>(a);
+  latent_upproj_kernel<<<dim3(a.H, bgroups), 256, kUpSmem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -118,15 +118,6 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-__device__ __forceinline__ void tma_load_3d_nohint(void* smem_dst, const void* tmap,
-                                                   uint64_t* bar, int c0, int c1, int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
-      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // One work unit: a pair of 128-row query tiles of one (b, h).  Units are numbered
 // heaviest first (the last query tiles see the most keys); CTA c of G takes units
 // i G + c in even rounds i and i G + (G - 1 - c) in odd ones, which balances the
@@ -771,6 +762,20 @@ cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream) {
   const size_t blocks = std::min<size_t>((n16 + 255) / 256, (size_t)(sms > 0 ? sms : 152) * 8);
   kv_append_kernel<<<(unsigned)std::max<size_t>(blocks, 1), 256, 0, stream>>>(a);
   return cudaGetLastError();
+}
+
+bool encode_bf16_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+                    uint64_t planes, uint64_t plane_rows, uint32_t box_rows) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {inner, rows, planes};
+  cuuint64_t strides[2] = {inner * 2, inner * 2 * plane_rows};
+  cuuint32_t box[3] = {64, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {

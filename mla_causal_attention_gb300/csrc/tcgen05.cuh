@@ -54,6 +54,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_ma
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// The same with the major-ness of A chosen too (bit 15: 1 = A MN-major).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_ab(int M, int N, bool a_mn_major,
+                                                        bool b_mn_major) {
+  return idesc_bf16_f32(M, N, b_mn_major) | ((a_mn_major ? 1u : 0u) << 15);
+}
+
 // One lane of a converged warp (elect.sync).  MMAs are issued by the elected lane while
 // the whole warp runs the issue loop, so descriptors and TMEM addresses stay warp-uniform.
 __device__ __forceinline__ bool elect_one() {

@@ -20,7 +20,8 @@ import torch
 
 from .workloads import Workload
 
-_TENSOR_IDS = {"q_nope": 1, "q_pe": 2, "k_nope": 3, "k_pe_shared": 4, "v": 5, "kv_len": 6}
+_TENSOR_IDS = {"q_nope": 1, "q_pe": 2, "k_nope": 3, "k_pe_shared": 4, "v": 5, "kv_len": 6,
+               "c_kv": 7, "w_kvb": 8}
 _MASK64 = (1 << 64) - 1
 
 
@@ -92,4 +93,32 @@ def make_inputs(wl: Workload, seed: int = 0, pin_memory: bool = False,
     if pin_memory:
         kv_len = kv_len.pin_memory()
     t.update(kv_len=kv_len, past_len=wl.past_len, softmax_scale=wl.softmax_scale, workload=wl)
+    return t
+
+
+def make_latent_inputs(wl: Workload, seed: int = 0, pin_memory: bool = False) -> dict:
+    """Inputs of decode over the latent cache for a decode workload (Tq = 1): q_nope
+    [B,H,128], q_pe [B,H,64], c_kv [B,Tk,512], k_pe [B,Tk,64] ~ N(0,1); the kv_b_proj weight
+    w_kvb [H*256,512] ~ N(0, 1/512), so the per-head keys and values it produces from the
+    latent rows are ~N(0,1) like the other workloads' inputs (synthetic: no trained
+    weights); kv_len drawn as for the workload."""
+    B, H, Tk = wl.B, wl.H, wl.Tk
+    t = {"q_nope": torch.empty((B, H, 128), dtype=torch.bfloat16),
+         "q_pe": torch.empty((B, H, 64), dtype=torch.bfloat16),
+         "c_kv": torch.empty((B, Tk, 512), dtype=torch.bfloat16),
+         "k_pe": torch.empty((B, Tk, 64), dtype=torch.bfloat16),
+         "w_kvb": torch.empty((H * 256, 512), dtype=torch.bfloat16)}
+    if pin_memory:
+        t = {k: v.pin_memory() for k, v in t.items()}
+    jobs = [(t["q_nope"][b], "q_nope", b, 0, 1.0) for b in range(B)]
+    jobs += [(t["q_pe"][b], "q_pe", b, 0, 1.0) for b in range(B)]
+    jobs += [(t["c_kv"][b], "c_kv", b, 0, 1.0) for b in range(B)]
+    jobs += [(t["k_pe"][b], "k_pe_shared", b, 0, 1.0) for b in range(B)]
+    jobs += [(t["w_kvb"][h * 256:(h + 1) * 256], "w_kvb", 0, h, 512 ** -0.5) for h in range(H)]
+    threads = min(32, os.cpu_count() or 1)
+    with ThreadPoolExecutor(threads) as ex:
+        list(ex.map(lambda j: _draw(j[0], seed, j[1], j[2], j[3], j[4]), jobs))
+    t["kv_len"] = draw_kv_len(wl, seed)
+    if pin_memory:
+        t["kv_len"] = t["kv_len"].pin_memory()
     return t

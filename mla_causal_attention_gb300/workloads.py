@@ -88,3 +88,22 @@ def algorithmic_bytes(wl: Workload, kv_len) -> int:
         total += keys * (H * (D_NOPE + D_V) + D_ROPE) * 2
         total += H * Tq * (D_NOPE + D_ROPE + D_V) * 2
     return total
+
+
+# Decode over the latent cache (the 512-wide kv_lora_rank latent rows plus the shared rotary
+# key, with the kv_b_proj up-projection absorbed): the two decode workloads above, served
+# from a latent cache instead of per-head keys and values.  Synthetic kv_b_proj weights.
+LATENT_WORKLOADS = {
+    "latent_decode_ragged": WORKLOADS["decode_ragged"],
+    "latent_decode_p1000": WORKLOADS["decode_p1000"],
+}
+D_LAT = 512
+
+
+def latent_algorithmic_bytes(wl: Workload, kv_len) -> int:
+    """Latent rows and rotary keys read once below kv_len (1152 bytes per key), q_nope,
+    q_pe and out once per (b, h), and the kv_b_proj weight once (H x 256 x 512 bf16)."""
+    kv = np.asarray(kv_len, dtype=np.int64).reshape(-1)
+    keys = int(np.minimum(kv, wl.Tk).sum())
+    return (keys * (D_LAT + D_ROPE) * 2 + wl.B * wl.H * (D_NOPE + D_ROPE + D_V) * 2
+            + wl.H * 256 * D_LAT * 2)
