@@ -50,7 +50,7 @@ constexpr int kLD = 512;          // latent width (kv_lora_rank)
 constexpr int kLSubK = 16384;     // 128 keys x 64 columns, bf16, 128-byte swizzled
 constexpr int kLSubQ = 8192;      // 64 heads x 64 columns
 constexpr int kLSlots = 8;        // latent sub-tile s of every key tile lives in slot s
-constexpr int kLThreads = 256;    // warp 0 producer, warp 1 MMA, warps 4-7 softmax
+constexpr int kLThreads = 384;    // warp 0 producer, warp 1 MMA, warps 4-11 softmax
 constexpr int kLOffQ = 0;                             // 9 sub-tiles: q_lat 0-511, q_pe
 constexpr int kLOffRing = kLOffQ + 9 * kLSubQ;        // 73728
 constexpr int kLOffP = kLOffRing + kLSlots * kLSubK;  // 204800: the tile's rotary keys
@@ -81,7 +81,7 @@ struct LBars {
   uint64_t pe_free;         // the previous tile's value mixes are done with P^T
   uint64_t q_full;
   uint64_t s_full;          // S^T of the tile in TMEM
-  uint64_t p_ready;         // P^T in shared memory, O^T rescaled (4 warp arrivals)
+  uint64_t p_ready;         // P^T in shared memory, O^T rescaled (8 warp arrivals)
   uint64_t o_done;          // last value mix done
   uint64_t mma_done;
   uint32_t tmem_base;
@@ -97,19 +97,19 @@ __device__ __forceinline__ void ldrain(uint64_t* bar, uint32_t parity) {
   }
 }
 
-// Barrier over the 4 softmax warps (named barrier 1) that ANDs a predicate across them.
+// Barrier over the 8 softmax warps (named barrier 1) that ANDs a predicate across them.
 __device__ __forceinline__ bool softmax_and(bool v) {
   uint32_t r;
   asm volatile(
       "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n"
-      " bar.red.and.pred po, 1, 128, pi;\n selp.u32 %0, 1, 0, po;\n}"
+      " bar.red.and.pred po, 1, 256, pi;\n selp.u32 %0, 1, 0, po;\n}"
       : "=r"(r)
       : "r"((uint32_t)v)
       : "memory");
   return r != 0;
 }
 __device__ __forceinline__ void softmax_sync() {
-  asm volatile("bar.sync 1, 128;" ::: "memory");
+  asm volatile("bar.sync 1, 256;" ::: "memory");
 }
 
 struct OpMax {
@@ -119,38 +119,34 @@ struct OpAdd {
   __device__ __forceinline__ float operator()(float a, float b) const { return a + b; }
 };
 
-// Reduces 64 per-head values over the 32 lanes of a warp by halving exchanges (31 x 2
-// shuffles instead of 64 x 5): lane l ends with the results for heads 2l and 2l + 1.
+// Reduces 32 per-head values over the 32 lanes of a warp by halving exchanges (31
+// shuffles instead of 32 x 5): lane l ends with the result for head l.
 template <class Op>
-__device__ __forceinline__ void halving_reduce64(const float (&v)[64], float (&out)[2],
-                                                 int lane, Op op) {
-  float a[32], c[16], d[8], e[4];
+__device__ __forceinline__ float halving_reduce32(const float (&v)[32], int lane, Op op) {
+  float c[16], d[8], e[4], f[2];
   const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2, b0 = lane & 1;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const float keep = b4 ? v[i + 32] : v[i], send = b4 ? v[i] : v[i + 32];
-    a[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
-  }
-#pragma unroll
   for (int i = 0; i < 16; ++i) {
-    const float keep = b3 ? a[i + 16] : a[i], send = b3 ? a[i] : a[i + 16];
-    c[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
+    const float keep = b4 ? v[i + 16] : v[i], send = b4 ? v[i] : v[i + 16];
+    c[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
   }
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const float keep = b2 ? c[i + 8] : c[i], send = b2 ? c[i] : c[i + 8];
-    d[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
+    const float keep = b3 ? c[i + 8] : c[i], send = b3 ? c[i] : c[i + 8];
+    d[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float keep = b1 ? d[i + 4] : d[i], send = b1 ? d[i] : d[i + 4];
-    e[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 2));
+    const float keep = b2 ? d[i + 4] : d[i], send = b2 ? d[i] : d[i + 4];
+    e[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
   }
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
-    const float keep = b0 ? e[i + 2] : e[i], send = b0 ? e[i] : e[i + 2];
-    out[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 1));
+    const float keep = b1 ? e[i + 2] : e[i], send = b1 ? e[i] : e[i + 2];
+    f[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 2));
   }
+  const float keep = b0 ? f[1] : f[0], send = b0 ? f[0] : f[1];
+  return op(keep, __shfl_xor_sync(0xffffffffu, send, 1));
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -191,7 +187,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
     mbar_init(&bars->pe_free, 1);
     mbar_init(&bars->q_full, 1);
     mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->p_ready, 4);
+    mbar_init(&bars->p_ready, 8);
     mbar_init(&bars->o_done, 1);
     mbar_init(&bars->mma_done, 1);
     bars->abort_flag = 0;
@@ -315,14 +311,19 @@ __global__ void __launch_bounds__(kLThreads, 1)
     ldrain(&bars->mma_done, 0);
   } else if (warp >= 4) {
     // ================= softmax warps =================
-    // Thread = key row r of the tile = TMEM lane r; its S^T row holds the 64 heads' scores.
-    const int sw = warp - 4;
+    // Two groups of 4 warps: group g owns heads [32g, 32g + 32).  Thread = key row r of the
+    // tile = TMEM lane r (warp % 4 selects the lane quarter); its 32 columns of the S^T row
+    // are its group's heads.  For the value pass, lane r is latent column 128q + r of O^T
+    // block q, and the group rescales its heads' columns.
+    const int grp = (warp - 4) >> 2;
+    const int hb = 32 * grp;
+    const int sw = warp & 3;
     const int r = sw * 32 + lane;
-    const int t = threadIdx.x - 128;  // owner of head t when t < 64
+    const int t = threadIdx.x - 128;  // owner of head t when t < 64 (warps 4, 5)
     const uint32_t lane_off = (uint32_t)(sw * 32) << 16;
-    const uint32_t s_t = tbase + lane_off;
-    const uint32_t o_t = tbase + lane_off + 64;
-    float* red_max = reinterpret_cast<float*>(smem + kLOffRed);  // [4 warps][64 heads]
+    const uint32_t s_t = tbase + lane_off + hb;
+    const uint32_t o_t = tbase + lane_off + 64 + hb;
+    float* red_max = reinterpret_cast<float*>(smem + kLOffRed);  // [4 quarters][64 heads]
     float* red_sum = red_max + 256;                               // [4][64]
     float* mbase = red_sum + 256;                                 // [64] exponent base
     float* alpha_s = mbase + 64;                                  // [64] this tile's rescale
@@ -335,27 +336,20 @@ __global__ void __launch_bounds__(kLThreads, 1)
     for (int j = 0; j < nt; ++j) {
       const bool got =
           __all_sync(0xffffffffu, mbar_wait(&bars->s_full, j & 1, p.status, abort_flag));
-      float v[64];
+      float v[32];
       if (got) {
         tc::fence_after_sync();
-        uint32_t ra[32], rb[32];
+        uint32_t ra[32];
         tc::tmem_ld32(s_t, ra);
-        tc::tmem_ld32(s_t + 32, rb);
         tc::tmem_wait_ld();
         const bool vis = j0 + j * kLatTile + r < j1;
 #pragma unroll
-        for (int h = 0; h < 32; ++h) {
-          v[h] = vis ? __uint_as_float(ra[h]) : -INFINITY;
-          v[h + 32] = vis ? __uint_as_float(rb[h]) : -INFINITY;
-        }
+        for (int h = 0; h < 32; ++h) v[h] = vis ? __uint_as_float(ra[h]) : -INFINITY;
       } else {
 #pragma unroll
-        for (int h = 0; h < 64; ++h) v[h] = -INFINITY;
+        for (int h = 0; h < 32; ++h) v[h] = -INFINITY;
       }
-      float w2[2];
-      halving_reduce64(v, w2, lane, OpMax());
-      red_max[sw * 64 + 2 * lane] = w2[0];
-      red_max[sw * 64 + 2 * lane + 1] = w2[1];
+      red_max[sw * 64 + hb + lane] = halving_reduce32(v, lane, OpMax());
       if (!softmax_and(got)) {  // barrier A; every warp leaves together on a failed wait
         ok = false;
         break;
@@ -378,39 +372,33 @@ __global__ void __launch_bounds__(kLThreads, 1)
         any_rescale[(j + 1) & 1] = 0;  // everyone read it before barrier A of this tile
       }
       softmax_sync();  // barrier B
-      float pv[64];
+      float pv[32];
 #pragma unroll
-      for (int h = 0; h < 64; h += 4) {
-        const float4 mb = *reinterpret_cast<const float4*>(mbase + h);
+      for (int h = 0; h < 32; h += 4) {
+        const float4 mb = *reinterpret_cast<const float4*>(mbase + hb + h);
         pv[h] = ex2_approx(fmaf(v[h], sl2, -mb.x));
         pv[h + 1] = ex2_approx(fmaf(v[h + 1], sl2, -mb.y));
         pv[h + 2] = ex2_approx(fmaf(v[h + 2], sl2, -mb.z));
         pv[h + 3] = ex2_approx(fmaf(v[h + 3], sl2, -mb.w));
       }
       if (any_rescale[j & 1]) {
-        // O^T columns of heads whose max grew: this thread's lane in each of the 4 blocks.
+        // O^T columns of this group's heads whose max grew, in each of the 4 blocks.
 #pragma unroll 1
         for (int q = 0; q < 4; ++q) {
+          uint32_t o[32];
+          tc::tmem_ld32(o_t + 64 * q, o);
+          tc::tmem_wait_ld();
 #pragma unroll
-          for (int hh = 0; hh < 64; hh += 32) {
-            uint32_t o[32];
-            tc::tmem_ld32(o_t + 64 * q + hh, o);
-            tc::tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha_s[hh + e]);
-            tc::tmem_st32(o_t + 64 * q + hh, o);
-          }
+          for (int e = 0; e < 32; ++e)
+            o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha_s[hb + e]);
+          tc::tmem_st32(o_t + 64 * q, o);
         }
         tc::tmem_wait_st();
       }
-      float s2[2];
-      halving_reduce64(pv, s2, lane, OpAdd());
-      red_sum[sw * 64 + 2 * lane] = s2[0];
-      red_sum[sw * 64 + 2 * lane + 1] = s2[1];
+      red_sum[sw * 64 + hb + lane] = halving_reduce32(pv, lane, OpAdd());
       // P^T [64 heads x 128 keys] bf16, 128-byte swizzled like a TMA tile: keys r and r ^ 1
-      // are lanes l and l ^ 1, so even lanes store heads 0-31 and odd lanes heads 32-63,
-      // each word holding the pair (key r & ~1, key r | 1).
+      // are lanes l and l ^ 1, so even lanes store the group's heads 0-15 and odd lanes its
+      // heads 16-31, each word holding the pair (key r & ~1, key r | 1).
       {
         const bool odd = lane & 1;
         const int kp = r & ~1;
@@ -418,11 +406,11 @@ __global__ void __launch_bounds__(kLThreads, 1)
         const int kin = kp & 63;
         const int chunk = (kin * 2) >> 4, within = (kin * 2) & 15;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float mine = odd ? pv[i + 32] : pv[i];
-          const float send = odd ? pv[i] : pv[i + 32];
+        for (int i = 0; i < 16; ++i) {
+          const float mine = odd ? pv[i + 16] : pv[i];
+          const float send = odd ? pv[i] : pv[i + 16];
           const float other = __shfl_xor_sync(0xffffffffu, send, 1);
-          const int h = odd ? i + 32 : i;
+          const int h = hb + (odd ? i + 16 : i);
           const uint32_t word = odd ? pack_bf16x2(other, mine) : pack_bf16x2(mine, other);
           *reinterpret_cast<uint32_t*>(pb + (h >> 3) * 1024 + (h & 7) * 128 +
                                        ((chunk ^ (h & 7)) << 4) + within) = word;
@@ -441,16 +429,14 @@ __global__ void __launch_bounds__(kLThreads, 1)
         const size_t row0 = (size_t)b * p.H * p.splits + split;  // (b, head 0, split)
 #pragma unroll 1
         for (int q = 0; q < 4; ++q) {
-          uint32_t oa[32], ob[32];
+          uint32_t oa[32];
           tc::tmem_ld32(o_t + 64 * q, oa);
-          tc::tmem_ld32(o_t + 64 * q + 32, ob);
           tc::tmem_wait_ld();
           const int d = 128 * q + r;
 #pragma unroll
-          for (int h = 0; h < 64; ++h) {
-            if (h < p.H)
-              p.part_acc[(row0 + (size_t)h * p.splits) * kLD + d] =
-                  __uint_as_float(h < 32 ? oa[h] : ob[h - 32]);
+          for (int h = 0; h < 32; ++h) {
+            if (hb + h < p.H)
+              p.part_acc[(row0 + (size_t)(hb + h) * p.splits) * kLD + d] = __uint_as_float(oa[h]);
           }
         }
         if (t < p.H)
