@@ -102,14 +102,15 @@ def kernel_source_sha():
     return h.hexdigest()
 
 
-def recorded_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if it matches this source."""
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this
+    workload with this source."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         e = d[kernel]
-        if e.get("source_sha256") != kernel_source_sha():
+        if e.get("source_sha256") != kernel_source_sha() or e.get("workload") != workload:
             return None
         return int(e["dram_bytes_per_launch"])
     except Exception:
@@ -273,7 +274,7 @@ def measure_ours(wl, args, rank, world, local, with_cpu):
         peak, peak_src = peak_for("tensor", bf16_sustained)
     achieved = m["work"] / (per_launch_ms * 1e-3) * m["scale"]
     kernel_name = "mla_prefill_kernel" if m["kind"] == "prefill" else "decode_splitkv_kernel"
-    traffic = recorded_traffic(kernel_name)
+    traffic = recorded_traffic(kernel_name, wl.name)
     res = {
         "value": value, "unit": m["unit"], "ms_per_step": ms,
         "step_ms_min": min(step_ms), "step_ms_max": max(step_ms),
@@ -352,7 +353,7 @@ def measure_latent(name, args, rank, world, local, with_cpu):
     res = {"workload": name, "value": whole_job_rate(work, world, ms, 1e-9), "unit": "GB/s",
            "ms_per_step": ms, "step_ms_min": min(step_ms), "step_ms_max": max(step_ms),
            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                        "frac": achieved / peak, "traffic": recorded_traffic("latent_splitkv_kernel"),
+                        "frac": achieved / peak, "traffic": recorded_traffic("latent_splitkv_kernel", name),
                         "peak_source": peak_src, "kernel": "latent path (4 kernels)",
                         "algorithmic_per_launch": work},
            "clocks": clk.summary(), "gpu_launches": 4 * args.steps,
