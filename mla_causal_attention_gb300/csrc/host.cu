@@ -98,7 +98,7 @@ size_t latent_acc_bytes(int B, int H, int splits) {
 }
 size_t latent_workspace(int B, int H, int splits) {
   return kStatusBytes + latent_q_bytes(B, H) + latent_ml_bytes(B, H, splits) +
-         latent_acc_bytes(B, H, splits) + r256((size_t)B * H * 512 * 4);
+         latent_acc_bytes(B, H, splits) + r256((size_t)B * H * 512 * 2);
 }
 
 // Rotary workspace: rotated queries [B,H,Tq,64] then rotated new rotary keys [B,Tq,64],
@@ -504,7 +504,7 @@ mla_status mla_latent_decode_fwd(const uint16_t* q_nope, const uint16_t* q_pe,
   cur += latent_ml_bytes(B, H, pl.splits);
   a.part_acc = reinterpret_cast<float*>(cur);
   cur += latent_acc_bytes(B, H, pl.splits);
-  a.o_lat = reinterpret_cast<float*>(cur);
+  a.o_lat = reinterpret_cast<uint16_t*>(cur);
   a.B = B; a.H = H; a.Tk = Tk; a.kv_rows = Tk; a.chunk = pl.chunk; a.splits = pl.splits;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   return launch_latent(a, static_cast<cudaStream_t>(cuda_stream)) == cudaSuccess ? MLA_OK

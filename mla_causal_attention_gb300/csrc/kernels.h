@@ -143,7 +143,7 @@ bool encode_bf16_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t r
 // Decode over the latent cache (absorbed kv_b_proj).  Shapes: q_nope [B,H,128], q_pe
 // [B,H,64], c_kv [B,kv_rows,512], k_pe [B,kv_rows,64], w_kvb [H*256,512]; out [B,H,128].
 // Workspace pieces (device): q_lat bf16 [B,H,512], part_ml f32 [B*H*splits][2], part_acc
-// f32 [B*H*splits][512], o_lat f32 [B,H,512].
+// f32 [B*H*splits][512], o_lat bf16 [B,H,512].
 struct LatentArgs {
   const uint16_t* q_nope;
   const uint16_t* q_pe;
@@ -155,7 +155,7 @@ struct LatentArgs {
   uint16_t* q_lat;
   float* part_ml;
   float* part_acc;
-  float* o_lat;
+  uint16_t* o_lat;
   int* status;
   int B, H, Tk, kv_rows, chunk, splits;
   float scale_log2;

@@ -155,6 +155,7 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 __global__ void __launch_bounds__(kLThreads, 1)
     latent_splitkv_kernel(const __grid_constant__ LatentParams p) {
+  grid_dep_launch();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -209,10 +210,6 @@ __global__ void __launch_bounds__(kLThreads, 1)
       prefetch_tmap(&p.tm_qr);
       prefetch_tmap(&p.tm_c);
       prefetch_tmap(&p.tm_kr);
-      mbar_arrive_expect_tx(&bars->q_full, 9 * kLSubQ);
-      for (int s = 0; s < 8; ++s)
-        tma_load_3d_nohint(sQ + s * kLSubQ, &p.tm_q, &bars->q_full, 64 * s, 0, b);
-      tma_load_3d_nohint(sQ + 8 * kLSubQ, &p.tm_qr, &bars->q_full, 0, 0, b);
       bool ok = true;
       int posted = 0;  // key tiles whose loads were issued
       for (int j = 0; j < nt && ok; ++j) {
@@ -228,6 +225,15 @@ __global__ void __launch_bounds__(kLThreads, 1)
                              b);
         }
         if (!ok) break;
+        if (j == 0) {
+          // The queries come from the absorb kernel, which may still be running (this grid
+          // can start early; its first latent loads do not depend on it).
+          grid_dep_wait();
+          mbar_arrive_expect_tx(&bars->q_full, 9 * kLSubQ);
+          for (int s = 0; s < 8; ++s)
+            tma_load_3d_nohint(sQ + s * kLSubQ, &p.tm_q, &bars->q_full, 64 * s, 0, b);
+          tma_load_3d_nohint(sQ + 8 * kLSubQ, &p.tm_qr, &bars->q_full, 0, 0, b);
+        }
         // Rotary keys into the P^T buffer once the previous tile's value mixes are done.
         if (j > 0) ok = mbar_wait(&bars->pe_free, prev, p.status, abort_flag);
         if (!ok) break;
@@ -455,10 +461,10 @@ __global__ void __launch_bounds__(kLThreads, 1)
 }
 
 // Warp-level bf16 MMA (m16n8k16, fp32 accumulate) for the two per-head projections: small
-// GEMMs (16 sequences x 128 or 512 columns x 512 or 128) whose operands sit in shared
-// memory.  Fragments (g = lane / 4, c = lane % 4): A a0 (row g, cols 2c, 2c+1), a1 (row
-// g+8), a2 (cols + 8), a3 (row g+8, cols + 8); B b0 (rows k = 2c, 2c+1, col g), b1 (k + 8);
-// C c0, c1 (row g, cols 2c, 2c+1), c2, c3 (row g+8).
+// GEMMs (64 sequences x 128 columns x 128, 64 x 32 x 512) whose operands sit in padded
+// shared memory and are read with ldmatrix.  Fragments (g = lane / 4, c = lane % 4): A a0
+// (row g, cols 2c, 2c+1), a1 (row g+8), a2 (cols + 8), a3 (row g+8, cols + 8); B b0 (rows
+// k = 2c, 2c+1, col g), b1 (k + 8); C c0, c1 (row g, cols 2c, 2c+1), c2, c3 (row g+8).
 __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
   asm volatile(
@@ -467,49 +473,62 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-
-constexpr int kWRow = kLD + 8;    // padded shared-memory row of W (bf16): conflict-free
-constexpr int kQRow = 128 + 8;    // padded row of 128 bf16
-constexpr int kAbsorbSmem = 128 * kWRow * 2 + 16 * kQRow * 2;
-constexpr int kUpSmem = 128 * kWRow * 2 + 16 * kWRow * 2;
-
-// Copies rows [row0, row0 + 128) of w_kvb (512 bf16 each) into padded shared memory with
-// asynchronous 16-byte copies (all in flight at once); the caller waits with
-// cp_async_wait_all and a block barrier.
-__device__ __forceinline__ void stage_w(uint16_t* sw, const uint16_t* w_kvb, size_t row0) {
-  const uint4* src = reinterpret_cast<const uint4*>(w_kvb + row0 * kLD);
-  for (int i = threadIdx.x; i < 128 * (kLD / 8); i += blockDim.x) {
-    const int r = i / (kLD / 8), c = i % (kLD / 8);
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
-                     smem_u32(sw + r * kWRow + c * 8)),
-                 "l"(src + i)
-                 : "memory");
-  }
-  asm volatile("cp.async.commit_group;" ::: "memory");
+// Four 8x8 bf16 matrices from shared memory; lane l gives the row address of matrix l / 8.
+__device__ __forceinline__ void ldsm4(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+// The same, each matrix transposed.
+__device__ __forceinline__ void ldsm4t(uint32_t (&r)[4], const void* p) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(smem_u32(p)));
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_all;" ::: "memory");
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
 }
 
-// q_lat[b,h,:] = W_K[h]^T q_nope[b,h]: per (head, 16 sequences) a [16 x 128] . [128 x 512]
-// GEMM; warp w computes latent columns [64w, 64w + 64).
+constexpr int kPB = 64;            // sequences per projection CTA
+constexpr int kAbN = 128;          // latent columns per absorb CTA
+constexpr int kAbRow = 128 + 8;    // padded bf16 row (128 values) of the absorb operands
+constexpr int kAbsorbSmem = (128 + kPB) * kAbRow * 2;
+constexpr int kUpN = 32;           // output columns per up-projection CTA
+constexpr int kUpRow = kLD + 8;    // padded bf16 row (512 values)
+constexpr int kUpSmem = (kUpN + kPB) * kUpRow * 2;
+
+// q_lat[b,h,n] = sum_k W_K[h][k][n] q_nope[b,h,k] for one head, a quarter of the 512 latent
+// columns and 64 sequences: [64 x 128] . [128 x 128].  W_K[h] = rows h*256 .. h*256+127 of
+// kv_b_proj (k = no-rope key dim, n = latent dim).  Warp w: row tile w % 4 (16 sequences),
+// columns 64 (w / 4) .. +63.
 __global__ void __launch_bounds__(256) latent_absorb_kernel(const LatentArgs a) {
+  grid_dep_launch();
   extern __shared__ __align__(16) uint8_t ab_smem[];
-  uint16_t* sw = reinterpret_cast<uint16_t*>(ab_smem);  // W_K[h]: 128 rows (k) x 512 (n)
-  uint16_t* sq = sw + 128 * kWRow;                       // q_nope: 16 rows (m) x 128 (k)
+  uint16_t* sw = reinterpret_cast<uint16_t*>(ab_smem);  // W_K slice: 128 rows (k) x 128 (n)
+  uint16_t* sq = sw + 128 * kAbRow;                      // q_nope: 64 rows (b) x 128 (k)
   const int h = blockIdx.x;
-  const int b0 = blockIdx.y * 16;
-  const int nb = min(16, a.B - b0);
-  stage_w(sw, a.w_kvb, (size_t)h * 256);
-  for (int i = threadIdx.x; i < 16 * 16; i += blockDim.x) {
+  const int n0 = blockIdx.y * kAbN;
+  const int b0 = blockIdx.z * kPB;
+  const int nb = min(kPB, a.B - b0);
+  for (int i = threadIdx.x; i < 128 * 16; i += blockDim.x) {
     const int r = i >> 4, c = i & 15;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (r < nb) v = reinterpret_cast<const uint4*>(a.q_nope + ((size_t)(b0 + r) * a.H + h) * 128)[c];
-    *reinterpret_cast<uint4*>(sq + r * kQRow + c * 8) = v;
+    cp_async16(sw + r * kAbRow + c * 8, a.w_kvb + ((size_t)h * 256 + r) * kLD + n0 + c * 8);
+  }
+  for (int i = threadIdx.x; i < kPB * 16; i += blockDim.x) {
+    const int r = i >> 4, c = i & 15;
+    if (r < nb)
+      cp_async16(sq + r * kAbRow + c * 8, a.q_nope + ((size_t)(b0 + r) * a.H + h) * 128 + c * 8);
+    else
+      *reinterpret_cast<uint4*>(sq + r * kAbRow + c * 8) = make_uint4(0u, 0u, 0u, 0u);
   }
   cp_async_wait_all();
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mt = warp & 3, nh = warp >> 2;
   const int g = lane >> 2, c2 = (lane & 3) * 2;
   float acc[8][4];
 #pragma unroll
@@ -517,34 +536,35 @@ __global__ void __launch_bounds__(256) latent_absorb_kernel(const LatentArgs a) 
 #pragma unroll
   for (int k0 = 0; k0 < 128; k0 += 16) {
     uint32_t af[4];
-    af[0] = *reinterpret_cast<const uint32_t*>(sq + g * kQRow + k0 + c2);
-    af[1] = *reinterpret_cast<const uint32_t*>(sq + (g + 8) * kQRow + k0 + c2);
-    af[2] = *reinterpret_cast<const uint32_t*>(sq + g * kQRow + k0 + c2 + 8);
-    af[3] = *reinterpret_cast<const uint32_t*>(sq + (g + 8) * kQRow + k0 + c2 + 8);
+    ldsm4(af, sq + (mt * 16 + (lane & 15)) * kAbRow + k0 + (lane >> 4) * 8);
 #pragma unroll
-    for (int n = 0; n < 8; ++n) {
-      const int col = warp * 64 + n * 8 + g;  // B[k][n] = W_K[k][col]: rows k, k + 1
-      const uint16_t* wk = sw + (k0 + c2) * kWRow + col;
-      const uint32_t b0 = (uint32_t)wk[0] | ((uint32_t)wk[kWRow] << 16);
-      const uint32_t b1 = (uint32_t)wk[8 * kWRow] | ((uint32_t)wk[9 * kWRow] << 16);
-      mma16816(acc[n], af, b0, b1);
+    for (int np = 0; np < 4; ++np) {
+      // B[k][n] row-major: transposed loads give two n-tiles' (b0, b1)
+      uint32_t bf[4];
+      ldsm4t(bf, sw + (k0 + (lane & 15)) * kAbRow + nh * 64 + np * 16 + (lane >> 4) * 8);
+      mma16816(acc[2 * np], af, bf[0], bf[1]);
+      mma16816(acc[2 * np + 1], af, bf[2], bf[3]);
     }
   }
 #pragma unroll
   for (int n = 0; n < 8; ++n) {
-    const int col = warp * 64 + n * 8 + c2;
-    if (g < nb)
-      *reinterpret_cast<uint32_t*>(a.q_lat + ((size_t)(b0 + g) * a.H + h) * kLD + col) =
+    const int col = n0 + nh * 64 + n * 8 + c2;
+    const int r = mt * 16 + g;
+    if (r < nb)
+      *reinterpret_cast<uint32_t*>(a.q_lat + ((size_t)(b0 + r) * a.H + h) * kLD + col) =
           pack_bf16x2(acc[n][0], acc[n][1]);
-    if (g + 8 < nb)
-      *reinterpret_cast<uint32_t*>(a.q_lat + ((size_t)(b0 + g + 8) * a.H + h) * kLD + col) =
+    if (r + 8 < nb)
+      *reinterpret_cast<uint32_t*>(a.q_lat + ((size_t)(b0 + r + 8) * a.H + h) * kLD + col) =
           pack_bf16x2(acc[n][2], acc[n][3]);
   }
 }
 
 // One warp per (b, h): o_lat = sum_s 2^(m_s - m) acc_s / sum_s 2^(m_s - m) l_s over the
-// splits that hold visible keys; lane owns columns 4 lane + 128 k, k = 0..3.
+// splits that hold visible keys, written as bf16 (the up-projection's MMA operand type);
+// lane owns columns 4 lane + 128 k, k = 0..3.
 __global__ void __launch_bounds__(256) latent_combine_kernel(const LatentArgs a) {
+  grid_dep_launch();
+  grid_dep_wait();
   const int w = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (w >= a.B * a.H) return;
@@ -553,86 +573,121 @@ __global__ void __launch_bounds__(256) latent_combine_kernel(const LatentArgs a)
   kvl = min(max(kvl, 1), a.Tk);
   const int n = (kvl + a.chunk - 1) / a.chunk;
   const size_t base = (size_t)w * a.splits;
+  const float2* ml = reinterpret_cast<const float2*>(a.part_ml) + base;
   float m = -INFINITY;
-  for (int s = lane; s < n; s += 32) m = fmaxf(m, a.part_ml[(base + s) * 2]);
+  for (int s = lane; s < n; s += 32) m = fmaxf(m, ml[s].x);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   float l = 0.f;
   float4 acc[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = 0; s < n; ++s) {
-    const float2 ml = *reinterpret_cast<const float2*>(a.part_ml + (base + s) * 2);
-    const float f = ex2_approx(ml.x - m);
-    l += f * ml.y;
+  const float4* src = reinterpret_cast<const float4*>(a.part_acc + base * kLD) + lane;
+  for (int s0 = 0; s0 < n; s0 += 32) {
+    // lane t holds the weight of split s0 + t
+    float f = 0.f;
+    if (s0 + lane < n) {
+      const float2 v = ml[s0 + lane];
+      f = ex2_approx(v.x - m);
+      l += f * v.y;
+    }
+    const int cnt = min(32, n - s0);
+    int s = 0;
+    for (; s + 2 <= cnt; s += 2) {  // two splits' rows in flight
+      float4 v[2][4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float4 v =
-          *reinterpret_cast<const float4*>(a.part_acc + (base + s) * kLD + 128 * k + 4 * lane);
-      acc[k].x = fmaf(f, v.x, acc[k].x);
-      acc[k].y = fmaf(f, v.y, acc[k].y);
-      acc[k].z = fmaf(f, v.z, acc[k].z);
-      acc[k].w = fmaf(f, v.w, acc[k].w);
+      for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[u][k] = src[(size_t)(s0 + s + u) * (kLD / 4) + 32 * k];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const float fu = __shfl_sync(0xffffffffu, f, s + u);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          acc[k].x = fmaf(fu, v[u][k].x, acc[k].x);
+          acc[k].y = fmaf(fu, v[u][k].y, acc[k].y);
+          acc[k].z = fmaf(fu, v[u][k].z, acc[k].z);
+          acc[k].w = fmaf(fu, v[u][k].w, acc[k].w);
+        }
+      }
+    }
+    if (s < cnt) {
+      const float fu = __shfl_sync(0xffffffffu, f, s);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float4 v = src[(size_t)(s0 + s) * (kLD / 4) + 32 * k];
+        acc[k].x = fmaf(fu, v.x, acc[k].x);
+        acc[k].y = fmaf(fu, v.y, acc[k].y);
+        acc[k].z = fmaf(fu, v.z, acc[k].z);
+        acc[k].w = fmaf(fu, v.w, acc[k].w);
+      }
     }
   }
-  const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    float4 o = acc[k];
-    o.x *= inv;
-    o.y *= inv;
-    o.z *= inv;
-    o.w *= inv;
-    *reinterpret_cast<float4*>(a.o_lat + (size_t)w * kLD + 128 * k + 4 * lane) = o;
-  }
+  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  uint16_t* dst = a.o_lat + (size_t)w * kLD + 4 * lane;
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    *reinterpret_cast<uint2*>(dst + 128 * k) =
+        make_uint2(pack_bf16x2(acc[k].x * inv, acc[k].y * inv),
+                   pack_bf16x2(acc[k].z * inv, acc[k].w * inv));
 }
 
-// out[b,h,:] = W_V[h] o_lat[b,h]: per (head, 16 sequences) a [16 x 512] . [512 x 128] GEMM
-// (o_lat rounded to bf16 as the MMA operand); warp w computes output columns [16w, 16w+16).
+// out[b,h,n] = sum_k W_V[h][n][k] o_lat[b,h,k] for one head, 32 of its 128 output columns
+// and 64 sequences: [64 x 512] . [512 x 32].  W_V[h] = rows h*256+128 .. h*256+255 of
+// kv_b_proj.  The weight slice is staged before waiting for the combine kernel.  Warp w:
+// row tile w % 4, output columns 16 (w / 4) .. +15.
 __global__ void __launch_bounds__(256) latent_upproj_kernel(const LatentArgs a) {
   extern __shared__ __align__(16) uint8_t up_smem[];
-  uint16_t* sw = reinterpret_cast<uint16_t*>(up_smem);  // W_V[h]: 128 rows (n) x 512 (k)
-  uint16_t* so = sw + 128 * kWRow;                       // o_lat: 16 rows (m) x 512 (k)
+  uint16_t* sw = reinterpret_cast<uint16_t*>(up_smem);  // W_V slice: 32 rows (n) x 512 (k)
+  uint16_t* so = sw + kUpN * kUpRow;                     // o_lat: 64 rows (b) x 512 (k)
   const int h = blockIdx.x;
-  const int b0 = blockIdx.y * 16;
-  const int nb = min(16, a.B - b0);
-  stage_w(sw, a.w_kvb, (size_t)h * 256 + 128);
-  for (int i = threadIdx.x; i < 16 * (kLD / 4); i += blockDim.x) {
-    const int r = i / (kLD / 4), c = i % (kLD / 4);
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (r < nb) v = reinterpret_cast<const float4*>(a.o_lat + ((size_t)(b0 + r) * a.H + h) * kLD)[c];
-    *reinterpret_cast<uint2*>(so + r * kWRow + c * 4) =
-        make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+  const int n0 = blockIdx.y * kUpN;
+  const int b0 = blockIdx.z * kPB;
+  const int nb = min(kPB, a.B - b0);
+  for (int i = threadIdx.x; i < kUpN * (kLD / 8); i += blockDim.x) {
+    const int r = i / (kLD / 8), c = i % (kLD / 8);
+    cp_async16(sw + r * kUpRow + c * 8,
+               a.w_kvb + ((size_t)h * 256 + 128 + n0 + r) * kLD + c * 8);
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  grid_dep_wait();
+  for (int i = threadIdx.x; i < kPB * (kLD / 8); i += blockDim.x) {
+    const int r = i / (kLD / 8), c = i % (kLD / 8);
+    if (r < nb)
+      cp_async16(so + r * kUpRow + c * 8, a.o_lat + ((size_t)(b0 + r) * a.H + h) * kLD + c * 8);
+    else
+      *reinterpret_cast<uint4*>(so + r * kUpRow + c * 8) = make_uint4(0u, 0u, 0u, 0u);
   }
   cp_async_wait_all();
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int mt = warp & 3, nq = warp >> 2;
   const int g = lane >> 2, c2 = (lane & 3) * 2;
   float acc[2][4];
 #pragma unroll
   for (int n = 0; n < 2; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-#pragma unroll 4
+#pragma unroll 8
   for (int k0 = 0; k0 < kLD; k0 += 16) {
-    uint32_t af[4];
-    af[0] = *reinterpret_cast<const uint32_t*>(so + g * kWRow + k0 + c2);
-    af[1] = *reinterpret_cast<const uint32_t*>(so + (g + 8) * kWRow + k0 + c2);
-    af[2] = *reinterpret_cast<const uint32_t*>(so + g * kWRow + k0 + c2 + 8);
-    af[3] = *reinterpret_cast<const uint32_t*>(so + (g + 8) * kWRow + k0 + c2 + 8);
-#pragma unroll
-    for (int n = 0; n < 2; ++n) {
-      const uint16_t* wr = sw + (warp * 16 + n * 8 + g) * kWRow + k0 + c2;  // B[k][n] = W_V[n][k]
-      mma16816(acc[n], af, *reinterpret_cast<const uint32_t*>(wr),
-               *reinterpret_cast<const uint32_t*>(wr + 8));
-    }
+    uint32_t af[4], bf[4];
+    ldsm4(af, so + (mt * 16 + (lane & 15)) * kUpRow + k0 + (lane >> 4) * 8);
+    // W_V rows are n with k contiguous (B column-major): matrices (n 0-7, k0), (n 0-7,
+    // k0+8), (n 8-15, k0), (n 8-15, k0+8)
+    ldsm4(bf, sw + (nq * 16 + (lane & 7) + ((lane >> 4) << 3)) * kUpRow + k0 +
+                   ((lane >> 3) & 1) * 8);
+    mma16816(acc[0], af, bf[0], bf[1]);
+    mma16816(acc[1], af, bf[2], bf[3]);
   }
 #pragma unroll
   for (int n = 0; n < 2; ++n) {
-    const int col = warp * 16 + n * 8 + c2;
-    if (g < nb)
-      *reinterpret_cast<uint32_t*>(a.out + ((size_t)(b0 + g) * a.H + h) * 128 + col) =
+    const int col = n0 + nq * 16 + n * 8 + c2;
+    const int r = mt * 16 + g;
+    if (r < nb)
+      *reinterpret_cast<uint32_t*>(a.out + ((size_t)(b0 + r) * a.H + h) * 128 + col) =
           pack_bf16x2(acc[n][0], acc[n][1]);
-    if (g + 8 < nb)
-      *reinterpret_cast<uint32_t*>(a.out + ((size_t)(b0 + g + 8) * a.H + h) * 128 + col) =
+    if (r + 8 < nb)
+      *reinterpret_cast<uint32_t*>(a.out + ((size_t)(b0 + r + 8) * a.H + h) * 128 + col) =
           pack_bf16x2(acc[n][2], acc[n][3]);
   }
 }
@@ -716,11 +771,32 @@ cudaError_t launch_latent(const LatentArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_device = dev;
   }
-  const unsigned bgroups = (unsigned)((a.B + 15) / 16);
-  latent_absorb_kernel<<<dim3(a.H, bgroups), 256, kAbsorbSmem, stream>>>(a);
-  latent_splitkv_kernel<<<dim3(a.splits, a.B), kLThreads, kLSmem, stream>>>(p);
-  latent_combine_kernel<<<(unsigned)((a.B * a.H + 7) / 8), 256, 0, stream>>>(a);
-  latent_upproj_kernel<<<dim3(a.H, bgroups), 256, kUpSmem, stream>>>(a);
+  const unsigned bgroups = (unsigned)((a.B + kPB - 1) / kPB);
+  latent_absorb_kernel<<<dim3(a.H, kLD / kAbN, bgroups), 256, kAbsorbSmem, stream>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // The other three start as programmatic dependents of the kernel before them.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(a.splits, a.B);
+  cfg.blockDim = dim3(kLThreads);
+  cfg.dynamicSmemBytes = kLSmem;
+  e = cudaLaunchKernelEx(&cfg, latent_splitkv_kernel, p);
+  if (e != cudaSuccess) return e;
+  cfg.gridDim = dim3((unsigned)((a.B * a.H + 7) / 8));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  e = cudaLaunchKernelEx(&cfg, latent_combine_kernel, a);
+  if (e != cudaSuccess) return e;
+  cfg.gridDim = dim3(a.H, 128 / kUpN, bgroups);
+  cfg.dynamicSmemBytes = kUpSmem;
+  e = cudaLaunchKernelEx(&cfg, latent_upproj_kernel, a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

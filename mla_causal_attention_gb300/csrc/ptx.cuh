@@ -95,6 +95,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
   }
 }
 
+// ---- programmatic dependent launch ----------------------------------------------------
+// The next kernel on the stream, launched with programmatic stream serialization, may start
+// once every block of this one has called grid_dep_launch (or exited); it must call
+// grid_dep_wait before reading anything this kernel writes.  Both are no-ops in a kernel
+// launched without the attribute.
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ---- bulk copies (async proxy) ----------------------------------------------------------
 // 1-D bulk copy global -> shared, completion counted in bytes on an mbarrier.  Both
 // addresses 16-byte aligned, size a multiple of 16.

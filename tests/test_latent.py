@@ -48,6 +48,8 @@ def _oracle(d, rows=None):
     (1, 64, 1001, None),       # the decode shape at cached length 1000
     (2, 16, 700, (200, 700)),  # fewer heads than the MMA's 64 columns
     (5, 64, 2000, (1, 2000)),  # one split per sequence on a busy GPU
+    (70, 8, 200, (1, 200)),    # more sequences than one projection block (64) holds
+    (1, 8, 8192, None),        # 64 one-tile splits: the combine's weights in two rounds
 ])
 def test_latent_matches_oracle(B, H, Tk, kv):
     d = _case(B, H, Tk, kv, seed=B * 100 + Tk)
