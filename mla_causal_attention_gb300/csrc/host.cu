@@ -73,32 +73,30 @@ size_t key_bits_bytes(int B, int Tk) {
   return ((size_t)B * ((Tk + 127) / 128) * 16 + 255) & ~(size_t)255;
 }
 
-// Latent-cache decode: keys per split in whole 128-key tiles.  One CTA per SM runs at a
-// time (its shared memory), and sequences of a ragged batch differ in length, so splits
-// are short enough (8 tiles) that the hardware scheduler balances a few waves of them;
-// a batch too small to fill the SMs splits further, down to one tile per split.  Each split
-// writes 64 heads x 512 fp32 partials, about 11% of an 8-tile split's input bytes.
+// Latent-cache decode: one CTA per SM (its shared memory allows no more), each taking an
+// equal share of all sequences' 128-key tiles (the kernel partitions them from kv_len on the
+// device), capped at the tiles there can be.  Each CTA writes one 64 heads x 512 fp32
+// partial per sequence it touches: at most grid + B partials.
 struct LatentPlan {
-  int chunk, splits;
+  int grid;
 };
 LatentPlan plan_latent(int B, int Tk, int sms) {
-  const int tiles = (Tk + kLatTile - 1) / kLatTile;
-  int per = std::min(tiles, 8);
-  while (per > 1 && (int64_t)B * ((tiles + per - 1) / per) < sms) per = (per + 1) / 2;
+  const int64_t tiles = (int64_t)B * ((Tk + kLatTile - 1) / kLatTile);
   LatentPlan pl;
-  pl.chunk = per * kLatTile;
-  pl.splits = (Tk + pl.chunk - 1) / pl.chunk;
+  pl.grid = (int)std::min<int64_t>(tiles, sms);
   return pl;
 }
 size_t r256(size_t x) { return (x + 255) & ~(size_t)255; }
 size_t latent_q_bytes(int B, int H) { return r256((size_t)B * H * 512 * 2); }
-size_t latent_ml_bytes(int B, int H, int splits) { return r256((size_t)B * H * splits * 8); }
-size_t latent_acc_bytes(int B, int H, int splits) {
-  return r256((size_t)B * H * splits * 512 * 4);
+size_t latent_tile0_bytes(int B) { return r256((size_t)(B + 1) * 4); }
+size_t latent_ml_bytes(int B, int H, int grid) { return r256((size_t)(grid + B) * H * 8); }
+size_t latent_acc_bytes(int B, int H, int grid) {
+  return r256((size_t)(grid + B) * H * 512 * 4);
 }
-size_t latent_workspace(int B, int H, int splits) {
-  return kStatusBytes + latent_q_bytes(B, H) + latent_ml_bytes(B, H, splits) +
-         latent_acc_bytes(B, H, splits) + r256((size_t)B * H * 512 * 2);
+size_t latent_workspace(int B, int H, int grid) {
+  return kStatusBytes + latent_q_bytes(B, H) + latent_tile0_bytes(B) +
+         latent_ml_bytes(B, H, grid) + latent_acc_bytes(B, H, grid) +
+         r256((size_t)B * H * 512 * 2);
 }
 
 // Rotary workspace: rotated queries [B,H,Tq,64] then rotated new rotary keys [B,Tq,64],
@@ -470,7 +468,7 @@ size_t mla_latent_workspace_bytes(int B, int H, int Tk) {
   if (B < 1 || H < 1 || H > 64 || Tk < 1) return 0;
   int sms = 0;
   if (check_device(&sms) != MLA_OK || sms <= 0) sms = 152;
-  return latent_workspace(B, H, plan_latent(B, Tk, sms).splits);
+  return latent_workspace(B, H, plan_latent(B, Tk, sms).grid);
 }
 
 mla_status mla_latent_decode_fwd(const uint16_t* q_nope, const uint16_t* q_pe,
@@ -491,7 +489,7 @@ mla_status mla_latent_decode_fwd(const uint16_t* q_nope, const uint16_t* q_pe,
   mla_status st = check_device(&sms);
   if (st != MLA_OK) return st;
   const LatentPlan pl = plan_latent(B, Tk, sms);
-  if (workspace_bytes < latent_workspace(B, H, pl.splits)) return MLA_ERR_WORKSPACE;
+  if (workspace_bytes < latent_workspace(B, H, pl.grid)) return MLA_ERR_WORKSPACE;
   uint8_t* w = static_cast<uint8_t*>(workspace);
   LatentArgs a{};
   a.q_nope = q_nope; a.q_pe = q_pe; a.c_kv = c_kv; a.k_pe = k_pe; a.w_kvb = w_kvb;
@@ -500,12 +498,14 @@ mla_status mla_latent_decode_fwd(const uint16_t* q_nope, const uint16_t* q_pe,
   uint8_t* cur = w + kStatusBytes;
   a.q_lat = reinterpret_cast<uint16_t*>(cur);
   cur += latent_q_bytes(B, H);
+  a.seq_tile0 = reinterpret_cast<int32_t*>(cur);
+  cur += latent_tile0_bytes(B);
   a.part_ml = reinterpret_cast<float*>(cur);
-  cur += latent_ml_bytes(B, H, pl.splits);
+  cur += latent_ml_bytes(B, H, pl.grid);
   a.part_acc = reinterpret_cast<float*>(cur);
-  cur += latent_acc_bytes(B, H, pl.splits);
+  cur += latent_acc_bytes(B, H, pl.grid);
   a.o_lat = reinterpret_cast<uint16_t*>(cur);
-  a.B = B; a.H = H; a.Tk = Tk; a.kv_rows = Tk; a.chunk = pl.chunk; a.splits = pl.splits;
+  a.B = B; a.H = H; a.Tk = Tk; a.kv_rows = Tk; a.grid = pl.grid;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   return launch_latent(a, static_cast<cudaStream_t>(cuda_stream)) == cudaSuccess ? MLA_OK
                                                                                   : MLA_ERR_CUDA;

@@ -23,11 +23,15 @@
 // The split kernel runs both MMAs transposed, with keys (and latent columns) on the
 // 128 TMEM lanes and the 64 heads as the N dimension:
 //   S^T[128 keys, 64 heads]   = K_tile[128, 576] . Q^T        A = K tile (K-major), B = Q
-//   O^T[512, 64 heads]       += C_tile^T[512, 128] . P^T      4 M-blocks of 128 latent
+//   O^T[512, 64 heads]       += C_tile^T[512, 128] . P       4 M-blocks of 128 latent
 //                                                             columns; A = the tile's
 //                                                             latent rows read MN-major,
-//                                                             B = P^T from shared memory
-// so O^T takes 4 x 64 TMEM columns (a head-major O would need all 512).  The tile's eight
+//                                                             B = P [keys, heads] from
+//                                                             shared memory (MN-major)
+//   L[128, 64 heads]         += 1[128, 128] . P              the row sums, A = ones in TMEM
+// so O^T takes 4 x 64 TMEM columns (a head-major O would need all 512), and the softmax
+// needs no sum reduction: every row of L holds the running sum of each head's (bf16)
+// weights, rescaled with O^T.  The tile's eight
 // 64-column latent sub-tiles stay in eight fixed slots from the score pass through the
 // value pass (latent sub-tile s of every tile lives in slot s); its rotary-key sub-tile is
 // loaded into the P^T buffer, which is free during the score pass.  Each value block
@@ -50,16 +54,18 @@ constexpr int kLD = 512;          // latent width (kv_lora_rank)
 constexpr int kLSubK = 16384;     // 128 keys x 64 columns, bf16, 128-byte swizzled
 constexpr int kLSubQ = 8192;      // 64 heads x 64 columns
 constexpr int kLSlots = 8;        // latent sub-tile s of every key tile lives in slot s
-constexpr int kLThreads = 384;    // warp 0 producer, warp 1 MMA, warps 4-11 softmax
+constexpr int kLThreads = 384;    // warps 0, 2 producers, warp 1 MMA, warps 4-11 softmax
 constexpr int kLOffQ = 0;                             // 9 sub-tiles: q_lat 0-511, q_pe
 constexpr int kLOffRing = kLOffQ + 9 * kLSubQ;        // 73728
 constexpr int kLOffP = kLOffRing + kLSlots * kLSubK;  // 204800: the tile's rotary keys
-                                                      // (16 KB), then P^T (2 sub-tiles)
+                                                      // (16 KB), then P [128 keys x 64]
 constexpr int kLOffRed = kLOffP + kLSubK;             // 221184: softmax scratch
 constexpr int kLOffBar = kLOffRed + 4096;             // 225280
 constexpr int kLSmem = kLOffBar + 256 + 1024;         // + barriers + alignment slack
 static_assert(kLSmem <= 232448, "shared memory per block");
 constexpr float kLRescale = 8.0f;  // log2 units, as in the prefill kernel
+// TMEM columns: S^T [0, 64), O^T blocks [64, 320), L [320, 384), the ones operand [384, 416).
+constexpr uint32_t kLColO = 64, kLColL = 320, kLColOnes = 384;
 
 struct LatentParams {
   CUtensorMap tm_q;   // q_lat {512, H, B}, boxes {64, 64, 1}
@@ -67,10 +73,11 @@ struct LatentParams {
   CUtensorMap tm_c;   // c_kv  {512, Tk, B}, boxes {64, 128, 1}
   CUtensorMap tm_kr;  // k_pe  {64, Tk, B},  boxes {64, 128, 1}
   const int32_t* kv_len;
+  int32_t* seq_tile0;  // [B + 1]: first tile of each sequence in the partition, then T
   float* part_ml;
   float* part_acc;
   int* status;
-  int B, H, Tk, chunk, splits;
+  int B, H, Tk;
   float scale_log2;
 };
 
@@ -78,11 +85,13 @@ struct LBars {
   uint64_t full[kLSlots];   // slot s holds the current tile's latent sub-tile s
   uint64_t empty[kLSlots];  // slot s released by the value block that read it
   uint64_t pe_full;         // the tile's rotary keys are in the P^T buffer
-  uint64_t pe_free;         // the previous tile's value mixes are done with P^T
+  uint64_t pe_free;         // the previous tile's value mixes are done with P
   uint64_t q_full;
+  uint64_t q_empty;         // the segment's last score MMA has read Q
   uint64_t s_full;          // S^T of the tile in TMEM
-  uint64_t p_ready;         // P^T in shared memory, O^T rescaled (8 warp arrivals)
-  uint64_t o_done;          // last value mix done
+  uint64_t p_ready;         // P in shared memory, O^T and L rescaled (8 warp arrivals)
+  uint64_t o_done;          // the segment's last value mix done
+  uint64_t o_free;          // O^T and L of the segment read out (8 warp arrivals)
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort_flag;
@@ -112,46 +121,50 @@ __device__ __forceinline__ void softmax_sync() {
   asm volatile("bar.sync 1, 256;" ::: "memory");
 }
 
-struct OpMax {
-  __device__ __forceinline__ float operator()(float a, float b) const { return fmaxf(a, b); }
-};
-struct OpAdd {
-  __device__ __forceinline__ float operator()(float a, float b) const { return a + b; }
-};
-
-// Reduces 32 per-head values over the 32 lanes of a warp by halving exchanges (31
-// shuffles instead of 32 x 5): lane l ends with the result for head l.
-template <class Op>
-__device__ __forceinline__ float halving_reduce32(const float (&v)[32], int lane, Op op) {
-  float c[16], d[8], e[4], f[2];
-  const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2, b0 = lane & 1;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float keep = b4 ? v[i + 16] : v[i], send = b4 ? v[i] : v[i + 16];
-    c[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 16));
-  }
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float keep = b3 ? c[i + 8] : c[i], send = b3 ? c[i] : c[i + 8];
-    d[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 8));
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float keep = b2 ? d[i + 4] : d[i], send = b2 ? d[i] : d[i + 4];
-    e[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 4));
-  }
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const float keep = b1 ? e[i + 2] : e[i], send = b1 ? e[i] : e[i + 2];
-    f[i] = op(keep, __shfl_xor_sync(0xffffffffu, send, 2));
-  }
-  const float keep = b0 ? f[1] : f[0], send = b0 ? f[0] : f[1];
-  return op(keep, __shfl_xor_sync(0xffffffffu, send, 1));
+// Maximum of v over the 32 lanes of the warp (every lane gets it).
+__device__ __forceinline__ float redux_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
 }
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+
+// The work partition.  Sequence b holds n_b = ceil(kv_len[b] / 128) key tiles; laid end to
+// end they form T tiles, and CTA c of G = min(gridDim.x, T) takes tiles [c T / G,
+// (c + 1) T / G), so every CTA gets T / G >= 1 tiles to within one (CTAs past G exit).  A CTA's range crosses sequence boundaries: it walks the
+// segments (one per sequence it touches) in order, and writes one partial per segment, at
+// index c + b (unique: the (c, b) pairs covered form a staircase, monotone in both).
+__device__ __forceinline__ int latent_tiles(const LatentParams& p, int b) {
+  const int kv = p.kv_len ? min(max(p.kv_len[b], 1), p.Tk) : p.Tk;
+  return (kv + kLatTile - 1) / kLatTile;
+}
+__device__ __forceinline__ int latent_kv(const LatentParams& p, int b) {
+  return p.kv_len ? min(max(p.kv_len[b], 1), p.Tk) : p.Tk;
+}
+
+// One segment of a CTA's range: sequence b, its keys [j0, j1), nt tiles.
+struct LSeg {
+  int b, j0, j1, nt;
+};
+// Walks the segments of [t0, t1): start at sequence b0 whose first tile is P0.
+struct LSegWalk {
+  int b, P, t0, t1;
+  __device__ __forceinline__ bool next(const LatentParams& p, LSeg& s) {
+    if (P >= t1 || b >= p.B) return false;
+    const int n = latent_tiles(p, b);
+    const int lo = max(t0, P), hi = min(t1, P + n);
+    s.b = b;
+    s.j0 = (lo - P) * kLatTile;
+    s.j1 = min(latent_kv(p, b), (hi - P) * kLatTile);
+    s.nt = hi - lo;
+    P += n;
+    ++b;
+    return true;
+  }
+};
 
 __global__ void __launch_bounds__(kLThreads, 1)
     latent_splitkv_kernel(const __grid_constant__ LatentParams p) {
@@ -164,21 +177,69 @@ __global__ void __launch_bounds__(kLThreads, 1)
   uint8_t* sP = smem + kLOffP;
   LBars* bars = reinterpret_cast<LBars*>(smem + kLOffBar);
   volatile int* abort_flag = &bars->abort_flag;
-
-  const int split = blockIdx.x;
-  const int b = blockIdx.y;
-  int kvl = p.kv_len ? p.kv_len[b] : p.Tk;
-  if (kvl < 1 || kvl > p.Tk) {
-    if (threadIdx.x == 0 && split == 0) set_status(p.status, MLA_ERR_KVLEN);
-    kvl = min(max(kvl, 1), p.Tk);
-  }
-  const int j0 = split * p.chunk;
-  if (j0 >= kvl) return;  // uniform: this split holds no visible key (the combine skips it)
-  const int j1 = min(j0 + p.chunk, kvl);
-  const int nt = (j1 - j0 + kLatTile - 1) / kLatTile;
-
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int c = blockIdx.x;
+
+  // ---- the partition: per-sequence tile counts, a block-wide scan, this CTA's range ----
+  int* scan = reinterpret_cast<int*>(smem + kLOffRed);  // [12] warp totals, [16..17] result
+  int T;  // tiles of all sequences
+  {
+    const int per = (p.B + kLThreads - 1) / kLThreads;
+    const int bs = min(p.B, (int)threadIdx.x * per), be = min(p.B, bs + per);
+    int mine = 0;
+    bool bad = false;
+    for (int bb = bs; bb < be; ++bb) {
+      if (p.kv_len && (p.kv_len[bb] < 1 || p.kv_len[bb] > p.Tk)) bad = true;
+      mine += latent_tiles(p, bb);
+    }
+    if (bad && c == 0) set_status(p.status, MLA_ERR_KVLEN);
+    int incl = mine;  // inclusive scan within the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) scan[warp] = incl;
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int w = 0; w < kLThreads / 32; ++w) {
+      const int v = scan[w];
+      if (w < warp) before += v;
+      total += v;
+    }
+    const int excl = before + incl - mine;  // first tile of sequence bs
+    const int G = min((int)gridDim.x, total);
+    const int t0 = (int)((int64_t)c * total / G);
+    if (excl <= t0 && t0 < excl + mine) {  // this thread's sequences hold tile t0
+      int P = excl;
+      for (int bb = bs; bb < be; ++bb) {
+        const int n = latent_tiles(p, bb);
+        if (P + n > t0) {
+          scan[16] = bb;
+          scan[17] = P;
+          break;
+        }
+        P += n;
+      }
+    }
+    if (c == 0) {  // the prefix array, for the combine
+      int P = excl;
+      for (int bb = bs; bb < be; ++bb) {
+        p.seq_tile0[bb] = P;
+        P += latent_tiles(p, bb);
+      }
+      if (threadIdx.x == 0) p.seq_tile0[p.B] = total;
+    }
+    T = total;
+    __syncthreads();
+  }
+  const int G = min((int)gridDim.x, T);
+  if (c >= G) return;  // uniform: no tiles for this CTA
+  const int t0 = (int)((int64_t)c * T / G), t1 = (int)((int64_t)(c + 1) * T / G);
+  const int b_first = scan[16], P_first = scan[17];
+  __syncthreads();  // the scan scratch is reused by the softmax warps
+
   if (threadIdx.x == 0) {
     for (int i = 0; i < kLSlots; ++i) {
       mbar_init(&bars->full[i], 1);
@@ -187,9 +248,11 @@ __global__ void __launch_bounds__(kLThreads, 1)
     mbar_init(&bars->pe_full, 1);
     mbar_init(&bars->pe_free, 1);
     mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 1);
     mbar_init(&bars->s_full, 1);
     mbar_init(&bars->p_ready, 8);
     mbar_init(&bars->o_done, 1);
+    mbar_init(&bars->o_free, 8);
     mbar_init(&bars->mma_done, 1);
     bars->abort_flag = 0;
     fence_barrier_init();
@@ -202,117 +265,156 @@ __global__ void __launch_bounds__(kLThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tbase = bars->tmem_base;
+  LSegWalk walk{b_first, P_first, t0, t1};
+  LSeg sg;
 
-  if (warp == 0) {
+  if (warp == 0 || warp == 2) {
+    // Two producer threads: one thread's TMA issue rate is well below what the SM takes in,
+    // and a tile's loads are issued in one burst once its slots free up.  Producer pi owns
+    // the latent slots s = pi (mod 2); producer 0 also loads Q, producer 1 the rotary keys.
+    const int pi = warp >> 1;
     if (lane == 0) {
-      // ================= TMA producer =================
+      // ================= TMA producers =================
       prefetch_tmap(&p.tm_q);
       prefetch_tmap(&p.tm_qr);
       prefetch_tmap(&p.tm_c);
       prefetch_tmap(&p.tm_kr);
       bool ok = true;
-      int posted = 0;  // key tiles whose loads were issued
-      for (int j = 0; j < nt && ok; ++j) {
-        const int jt = j0 + j * kLatTile;
-        const uint32_t prev = (uint32_t)(j - 1) & 1u;
-        // Latent columns 0-511: sub-tile s into slot s once the previous tile's value block
-        // s / 2 has released it.
-        for (int sidx = 0; sidx < kLSlots; ++sidx) {
-          if (j > 0) ok = mbar_wait(&bars->empty[sidx], prev, p.status, abort_flag);
+      uint32_t g = 0;  // key tiles issued over the run
+      int nseg = 0;    // segments whose Q was issued
+      while (ok && walk.next(p, sg)) {
+        for (int j = 0; j < sg.nt && ok; ++j, ++g) {
+          const int jt = sg.j0 + j * kLatTile;
+          const uint32_t prev = (g - 1) & 1u;
+          // Latent columns 0-511: sub-tile s into slot s once the previous tile's value
+          // block s / 2 has released it.
+          for (int sidx = pi; sidx < kLSlots; sidx += 2) {
+            if (g > 0) ok = mbar_wait(&bars->empty[sidx], prev, p.status, abort_flag);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&bars->full[sidx], kLSubK);
+            tma_load_3d_nohint(sRing + sidx * kLSubK, &p.tm_c, &bars->full[sidx], 64 * sidx,
+                               jt, sg.b);
+          }
           if (!ok) break;
-          mbar_arrive_expect_tx(&bars->full[sidx], kLSubK);
-          tma_load_3d_nohint(sRing + sidx * kLSubK, &p.tm_c, &bars->full[sidx], 64 * sidx, jt,
-                             b);
+          if (j == 0 && pi == 0) {
+            // The segment's queries, once the previous segment's last score MMA has read
+            // Q.  They come from the absorb kernel, which may still be running (this grid
+            // can start early; the latent loads above do not depend on it).
+            if (nseg > 0) ok = mbar_wait(&bars->q_empty, (nseg - 1) & 1, p.status, abort_flag);
+            if (!ok) break;
+            if (nseg == 0) grid_dep_wait();
+            mbar_arrive_expect_tx(&bars->q_full, 9 * kLSubQ);
+            for (int s = 0; s < 8; ++s)
+              tma_load_3d_nohint(sQ + s * kLSubQ, &p.tm_q, &bars->q_full, 64 * s, 0, sg.b);
+            tma_load_3d_nohint(sQ + 8 * kLSubQ, &p.tm_qr, &bars->q_full, 0, 0, sg.b);
+            ++nseg;
+          }
+          // Rotary keys into the P buffer once the previous tile's value mixes are done.
+          if (pi == 1) {
+            if (g > 0) ok = mbar_wait(&bars->pe_free, prev, p.status, abort_flag);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&bars->pe_full, kLSubK);
+            tma_load_3d_nohint(sP, &p.tm_kr, &bars->pe_full, 0, jt, sg.b);
+          }
         }
-        if (!ok) break;
-        if (j == 0) {
-          // The queries come from the absorb kernel, which may still be running (this grid
-          // can start early; its first latent loads do not depend on it).
-          grid_dep_wait();
-          mbar_arrive_expect_tx(&bars->q_full, 9 * kLSubQ);
-          for (int s = 0; s < 8; ++s)
-            tma_load_3d_nohint(sQ + s * kLSubQ, &p.tm_q, &bars->q_full, 64 * s, 0, b);
-          tma_load_3d_nohint(sQ + 8 * kLSubQ, &p.tm_qr, &bars->q_full, 0, 0, b);
-        }
-        // Rotary keys into the P^T buffer once the previous tile's value mixes are done.
-        if (j > 0) ok = mbar_wait(&bars->pe_free, prev, p.status, abort_flag);
-        if (!ok) break;
-        mbar_arrive_expect_tx(&bars->pe_full, kLSubK);
-        tma_load_3d_nohint(sP, &p.tm_kr, &bars->pe_full, 0, jt, b);
-        posted = j + 1;
       }
       // Every load issued must land before shared memory is released: each barrier has at
-      // most its last phase in flight.
-      ldrain(&bars->q_full, 0);
-      if (posted > 0) {
-        for (int sidx = 0; sidx < kLSlots; ++sidx)
-          ldrain(&bars->full[sidx], (uint32_t)(posted - 1) & 1u);
-        ldrain(&bars->pe_full, (uint32_t)(posted - 1) & 1u);
+      // most its last phase in flight.  (A tile whose loads were only partly issued after a
+      // failed wait leaves its remaining slots one phase behind: their drains end at the
+      // wait limit, after the abort that caused them.)
+      if (pi == 0 && nseg > 0) ldrain(&bars->q_full, (uint32_t)(nseg - 1) & 1u);
+      if (g > 0) {
+        for (int sidx = pi; sidx < kLSlots; sidx += 2)
+          ldrain(&bars->full[sidx], (g - 1) & 1u);
+        if (pi == 1) ldrain(&bars->pe_full, (g - 1) & 1u);
       }
     }
   } else if (warp == 1) {
     // ================= MMA issuer =================
     constexpr uint32_t kIdQK = tc::idesc_bf16_f32_ab(128, 64, false, false);
-    constexpr uint32_t kIdPV = tc::idesc_bf16_f32_ab(128, 64, true, false);
+    constexpr uint32_t kIdPV = tc::idesc_bf16_f32_ab(128, 64, true, true);
+    constexpr uint32_t kIdL = tc::idesc_bf16_f32_ab(128, 64, false, true);
+    // P [keys, heads]: one 128-byte row per key, 8-key groups 1024 B apart (N = 64 spans a
+    // single swizzle atom, so the leading offset is unused).
+    const uint64_t dhi_p = tc::smem_desc_sw128(0, 16, 1024);
     const uint64_t dhi_k = tc::smem_desc_sw128(0, 16, 1024);
     const uint64_t dhi_mn = tc::smem_desc_sw128(0, kLSubK, 1024);  // slots 2q, 2q+1 adjacent
     const uint32_t q_lo = smem_u32(sQ) >> 4;
     const uint32_t ring_lo = smem_u32(sRing) >> 4;
     const uint32_t p_lo = smem_u32(sP) >> 4;
-    const uint32_t s_tmem = tbase;       // S^T: 64 columns
-    const uint32_t o_tmem = tbase + 64;  // O^T: 4 blocks of 64 columns
-    bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_full, 0, p.status, abort_flag));
-    tc::fence_after_sync();
-    for (int j = 0; j < nt && ok; ++j) {
-      const uint32_t ph = (uint32_t)j & 1u;
-      // S^T = K_tile Q^T over 576 columns: 4 k-steps of 16 per 64-column sub-tile; the
-      // rotary-key sub-tile (in the P^T buffer) last.
-      for (int sidx = 0; sidx < 9; ++sidx) {
-        uint64_t* fb = sidx < 8 ? &bars->full[sidx] : &bars->pe_full;
-        ok = __all_sync(0xffffffffu, mbar_wait(fb, ph, p.status, abort_flag));
+    const uint32_t s_tmem = tbase;            // S^T: 64 columns
+    const uint32_t o_tmem = tbase + kLColO;   // O^T: 4 blocks of 64 columns
+    const uint32_t l_tmem = tbase + kLColL;   // L: 64 columns
+    const uint32_t ones_tmem = tbase + kLColOnes;
+    bool ok = true;
+    uint32_t g = 0;  // key tiles over the run
+    int ns = 0;      // segments
+    while (ok && walk.next(p, sg)) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->q_full, ns & 1, p.status, abort_flag));
+      if (!ok) break;
+      tc::fence_after_sync();
+      for (int j = 0; j < sg.nt && ok; ++j, ++g) {
+        const uint32_t ph = g & 1u;
+        // S^T = K_tile Q^T over 576 columns: 4 k-steps of 16 per 64-column sub-tile; the
+        // rotary-key sub-tile (in the P buffer) last.
+        for (int sidx = 0; sidx < 9; ++sidx) {
+          uint64_t* fb = sidx < 8 ? &bars->full[sidx] : &bars->pe_full;
+          ok = __all_sync(0xffffffffu, mbar_wait(fb, ph, p.status, abort_flag));
+          if (!ok) break;
+          tc::fence_after_sync();
+          const uint32_t a_lo = sidx < 8 ? ring_lo + sidx * (kLSubK >> 4) : p_lo;
+          if (tc::elect_one()) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint32_t koff = kk * (32 >> 4);
+              const uint64_t adesc = dhi_k | (uint64_t)(a_lo + koff);
+              const uint64_t bdesc = dhi_k | (uint64_t)(q_lo + sidx * (kLSubQ >> 4) + koff);
+              tc::mma_ss(s_tmem, adesc, bdesc, kIdQK, (sidx | kk) != 0 ? 1u : 0u);
+            }
+            if (sidx == 8) {
+              tc::commit(&bars->s_full);
+              if (j == sg.nt - 1) tc::commit(&bars->q_empty);  // segment's last read of Q
+            }
+          }
+          __syncwarp();
+        }
+        if (!ok) break;
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->p_ready, ph, p.status, abort_flag));
+        // The segment's first value mix overwrites O^T and L: the previous segment's must
+        // have been read out.
+        if (ok && j == 0 && ns > 0)
+          ok = mbar_wait(&bars->o_free, (ns - 1) & 1, p.status, abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc::fence_after_sync();
-        const uint32_t a_lo = sidx < 8 ? ring_lo + sidx * (kLSubK >> 4) : p_lo;
+        // O^T block q (latent columns 128q..128q+127) += C_tile^T P over the tile's keys:
+        // A = slots 2q and 2q + 1 read MN-major, B = P; then L += 1 P (A = ones in TMEM).
         if (tc::elect_one()) {
+#pragma unroll 1
+          for (int q = 0; q < 4; ++q) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t koff = kk * (32 >> 4);
-            const uint64_t adesc = dhi_k | (uint64_t)(a_lo + koff);
-            const uint64_t bdesc = dhi_k | (uint64_t)(q_lo + sidx * (kLSubQ >> 4) + koff);
-            tc::mma_ss(s_tmem, adesc, bdesc, kIdQK, (sidx | kk) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t adesc =
+                  dhi_mn | (uint64_t)(ring_lo + 2 * q * (kLSubK >> 4) + kk * (2048 >> 4));
+              const uint64_t bdesc = dhi_p | (uint64_t)(p_lo + kk * (2048 >> 4));
+              tc::mma_ss(o_tmem + 64 * q, adesc, bdesc, kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            tc::commit(&bars->empty[2 * q]);
+            tc::commit(&bars->empty[2 * q + 1]);
           }
-          if (sidx == 8) tc::commit(&bars->s_full);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t bdesc = dhi_p | (uint64_t)(p_lo + kk * (2048 >> 4));
+            tc::mma_ts(l_tmem, ones_tmem, bdesc, kIdL, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc::commit(&bars->pe_free);
+          if (j == sg.nt - 1) tc::commit(&bars->o_done);
         }
         __syncwarp();
       }
-      if (!ok) break;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->p_ready, ph, p.status, abort_flag));
-      if (!ok) break;
-      tc::fence_after_sync();
-      // O^T block q (latent columns 128q..128q+127) += C_tile^T P^T over the tile's keys:
-      // A = slots 2q and 2q + 1 read MN-major, B = P^T.
-      if (tc::elect_one()) {
-#pragma unroll 1
-        for (int q = 0; q < 4; ++q) {
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t adesc =
-                dhi_mn | (uint64_t)(ring_lo + 2 * q * (kLSubK >> 4) + kk * (2048 >> 4));
-            const uint64_t bdesc =
-                dhi_k | (uint64_t)(p_lo + (kk >> 2) * (kLSubQ >> 4) + (kk & 3) * (32 >> 4));
-            tc::mma_ss(o_tmem + 64 * q, adesc, bdesc, kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
-          }
-          tc::commit(&bars->empty[2 * q]);
-          tc::commit(&bars->empty[2 * q + 1]);
-        }
-        tc::commit(&bars->pe_free);
-      }
-      __syncwarp();
+      ++ns;
     }
-    if (tc::elect_one()) {
-      if (ok) tc::commit(&bars->o_done);
-      tc::commit(&bars->mma_done);
-    }
+    if (tc::elect_one()) tc::commit(&bars->mma_done);
     __syncwarp();
     ldrain(&bars->mma_done, 0);
   } else if (warp >= 4) {
@@ -320,7 +422,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
     // Two groups of 4 warps: group g owns heads [32g, 32g + 32).  Thread = key row r of the
     // tile = TMEM lane r (warp % 4 selects the lane quarter); its 32 columns of the S^T row
     // are its group's heads.  For the value pass, lane r is latent column 128q + r of O^T
-    // block q, and the group rescales its heads' columns.
+    // block q (and row r of L), and the group rescales its heads' columns.
     const int grp = (warp - 4) >> 2;
     const int hb = 32 * grp;
     const int sw = warp & 3;
@@ -328,127 +430,151 @@ __global__ void __launch_bounds__(kLThreads, 1)
     const int t = threadIdx.x - 128;  // owner of head t when t < 64 (warps 4, 5)
     const uint32_t lane_off = (uint32_t)(sw * 32) << 16;
     const uint32_t s_t = tbase + lane_off + hb;
-    const uint32_t o_t = tbase + lane_off + 64 + hb;
+    const uint32_t o_t = tbase + lane_off + kLColO + hb;
+    const uint32_t l_t = tbase + lane_off + kLColL + hb;
     float* red_max = reinterpret_cast<float*>(smem + kLOffRed);  // [4 quarters][64 heads]
-    float* red_sum = red_max + 256;                               // [4][64]
-    float* mbase = red_sum + 256;                                 // [64] exponent base
+    float* mbase = red_max + 256;                                 // [64] exponent base
     float* alpha_s = mbase + 64;                                  // [64] this tile's rescale
     int* any_rescale = reinterpret_cast<int*>(alpha_s + 64);      // [2], by tile parity
     const float sl2 = p.scale_log2;
-    float m_own = -INFINITY, l_own = 0.f;  // running max (log2 units) and sum of head t
     if (t < 2) any_rescale[t] = 0;
+    if (grp == 0) {
+      // The all-ones A operand of the row-sum MMA (bf16 1.0 pairs), 32 columns.
+      uint32_t one[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) one[i] = 0x3F803F80u;
+      tc::tmem_st32(tbase + lane_off + kLColOnes, one);
+      tc::tmem_wait_st();
+    }
     softmax_sync();
     bool ok = true;
-    for (int j = 0; j < nt; ++j) {
-      const bool got =
-          __all_sync(0xffffffffu, mbar_wait(&bars->s_full, j & 1, p.status, abort_flag));
-      float v[32];
-      if (got) {
-        tc::fence_after_sync();
-        uint32_t ra[32];
-        tc::tmem_ld32(s_t, ra);
-        tc::tmem_wait_ld();
-        const bool vis = j0 + j * kLatTile + r < j1;
-#pragma unroll
-        for (int h = 0; h < 32; ++h) v[h] = vis ? __uint_as_float(ra[h]) : -INFINITY;
-      } else {
-#pragma unroll
-        for (int h = 0; h < 32; ++h) v[h] = -INFINITY;
-      }
-      red_max[sw * 64 + hb + lane] = halving_reduce32(v, lane, OpMax());
-      if (!softmax_and(got)) {  // barrier A; every warp leaves together on a failed wait
-        ok = false;
-        break;
-      }
-      if (t < 64) {
-        const float tm = fmaxf(fmaxf(red_max[t], red_max[64 + t]),
-                               fmaxf(red_max[128 + t], red_max[192 + t])) * sl2;
-        float a = 1.f;
-        if (j == 0) {
-          m_own = tm;  // key j0 < kv_len is visible: finite
-        } else if (tm > m_own + kLRescale) {
-          a = ex2_approx(m_own - tm);
-          m_own = tm;
-          l_own *= a;
-        }
-        mbase[t] = m_own;
-        alpha_s[t] = a;
-        if (a != 1.f) any_rescale[j & 1] = 1;
-      } else if (t == 64) {
-        any_rescale[(j + 1) & 1] = 0;  // everyone read it before barrier A of this tile
-      }
-      softmax_sync();  // barrier B
-      float pv[32];
-#pragma unroll
-      for (int h = 0; h < 32; h += 4) {
-        const float4 mb = *reinterpret_cast<const float4*>(mbase + hb + h);
-        pv[h] = ex2_approx(fmaf(v[h], sl2, -mb.x));
-        pv[h + 1] = ex2_approx(fmaf(v[h + 1], sl2, -mb.y));
-        pv[h + 2] = ex2_approx(fmaf(v[h + 2], sl2, -mb.z));
-        pv[h + 3] = ex2_approx(fmaf(v[h + 3], sl2, -mb.w));
-      }
-      if (any_rescale[j & 1]) {
-        // O^T columns of this group's heads whose max grew, in each of the 4 blocks.
-#pragma unroll 1
-        for (int q = 0; q < 4; ++q) {
-          uint32_t o[32];
-          tc::tmem_ld32(o_t + 64 * q, o);
+    uint32_t g = 0;  // key tiles over the run
+    int ns = 0;      // segments
+    while (ok && walk.next(p, sg)) {
+      float m_own = -INFINITY;  // running max (log2 units) of head t in this segment
+      for (int j = 0; j < sg.nt; ++j, ++g) {
+        const bool got =
+            __all_sync(0xffffffffu, mbar_wait(&bars->s_full, g & 1, p.status, abort_flag));
+        float v[32];
+        if (got) {
+          tc::fence_after_sync();
+          uint32_t ra[32];
+          tc::tmem_ld32(s_t, ra);
           tc::tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 32; ++e)
-            o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha_s[hb + e]);
-          tc::tmem_st32(o_t + 64 * q, o);
-        }
-        tc::tmem_wait_st();
-      }
-      red_sum[sw * 64 + hb + lane] = halving_reduce32(pv, lane, OpAdd());
-      // P^T [64 heads x 128 keys] bf16, 128-byte swizzled like a TMA tile: keys r and r ^ 1
-      // are lanes l and l ^ 1, so even lanes store the group's heads 0-15 and odd lanes its
-      // heads 16-31, each word holding the pair (key r & ~1, key r | 1).
-      {
-        const bool odd = lane & 1;
-        const int kp = r & ~1;
-        uint8_t* pb = sP + (kp >> 6) * kLSubQ;
-        const int kin = kp & 63;
-        const int chunk = (kin * 2) >> 4, within = (kin * 2) & 15;
+          for (int h = 0; h < 32; ++h) v[h] = __uint_as_float(ra[h]);
+          if (sg.j0 + j * kLatTile + r >= sg.j1) {  // key past the segment or past kv_len
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float mine = odd ? pv[i + 16] : pv[i];
-          const float send = odd ? pv[i] : pv[i + 16];
-          const float other = __shfl_xor_sync(0xffffffffu, send, 1);
-          const int h = hb + (odd ? i + 16 : i);
-          const uint32_t word = odd ? pack_bf16x2(other, mine) : pack_bf16x2(mine, other);
-          *reinterpret_cast<uint32_t*>(pb + (h >> 3) * 1024 + (h & 7) * 128 +
-                                       ((chunk ^ (h & 7)) << 4) + within) = word;
+            for (int h = 0; h < 32; ++h) v[h] = -INFINITY;
+          }
+        } else {
+#pragma unroll
+          for (int h = 0; h < 32; ++h) v[h] = -INFINITY;
         }
+        // Per-head maximum over this warp's 32 keys (warp-uniform results).
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 m4 = make_float4(redux_max(v[4 * i]), redux_max(v[4 * i + 1]),
+                                        redux_max(v[4 * i + 2]), redux_max(v[4 * i + 3]));
+          if (lane == 0) reinterpret_cast<float4*>(red_max + sw * 64 + hb)[i] = m4;
+        }
+        if (!softmax_and(got)) {  // barrier A; every warp leaves together on a failed wait
+          ok = false;
+          break;
+        }
+        if (t < 64) {
+          const float tm = fmaxf(fmaxf(red_max[t], red_max[64 + t]),
+                                 fmaxf(red_max[128 + t], red_max[192 + t])) * sl2;
+          float a = 1.f;
+          if (j == 0) {
+            m_own = tm;  // key j0 < kv_len is visible: finite
+          } else if (tm > m_own + kLRescale) {
+            a = ex2_approx(m_own - tm);
+            m_own = tm;
+          }
+          mbase[t] = m_own;
+          alpha_s[t] = a;
+          if (a != 1.f) any_rescale[g & 1] = 1;
+        } else if (t == 64) {
+          any_rescale[(g + 1) & 1] = 0;  // everyone read it before barrier A of this tile
+        }
+        softmax_sync();  // barrier B
+        // p = 2^(s * scale * log2(e) - m), two heads per packed fma
+        uint32_t pk[16];
+#pragma unroll
+        for (int h = 0; h < 32; h += 4) {
+          const float4 mb = *reinterpret_cast<const float4*>(mbase + hb + h);
+          const uint64_t sl2_2 = f2_pack(sl2, sl2);
+          float x0, x1, x2, x3;
+          f2_unpack(ffma2(f2_pack(v[h], v[h + 1]), sl2_2, f2_pack(-mb.x, -mb.y)), x0, x1);
+          f2_unpack(ffma2(f2_pack(v[h + 2], v[h + 3]), sl2_2, f2_pack(-mb.z, -mb.w)), x2, x3);
+          pk[h >> 1] = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
+          pk[(h >> 1) + 1] = pack_bf16x2(ex2_approx(x2), ex2_approx(x3));
+        }
+        if (any_rescale[g & 1]) {
+          // O^T and L columns of this group's heads whose max grew.
+#pragma unroll 1
+          for (int q = 0; q < 5; ++q) {
+            const uint32_t col = q < 4 ? o_t + 64 * q : l_t;
+            uint32_t o[32];
+            tc::tmem_ld32(col, o);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha_s[hb + e]);
+            tc::tmem_st32(col, o);
+          }
+          tc::tmem_wait_st();
+        }
+        // P [128 keys x 64 heads] bf16, 128-byte swizzled like a TMA tile: key r's row holds
+        // this group's 32 heads in 16-byte chunks 4g .. 4g + 3.
+        {
+          uint8_t* row = sP + r * 128;
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc)
+            *reinterpret_cast<uint4*>(row + (((4 * grp + cc) ^ (r & 7)) << 4)) =
+                make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+        }
+        fence_proxy_async_smem();  // P written by threads, read by the tensor core
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->p_ready);
       }
-      fence_proxy_async_smem();  // P^T written by threads, read by the tensor core
-      tc::fence_before_sync();
-      softmax_sync();  // barrier C
-      if (t < 64) l_own += (red_sum[t] + red_sum[64 + t]) + (red_sum[128 + t] + red_sum[192 + t]);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->p_ready);
-    }
-    if (ok) {
-      if (__all_sync(0xffffffffu, mbar_wait(&bars->o_done, 0, p.status, abort_flag))) {
+      if (!ok) break;
+      // The segment's partial: O^T and the row sums once its last value mix has run, at
+      // partial index c + b; then O^T and L are released for the next segment.
+      if (__all_sync(0xffffffffu, mbar_wait(&bars->o_done, ns & 1, p.status, abort_flag))) {
         tc::fence_after_sync();
-        const size_t row0 = (size_t)b * p.H * p.splits + split;  // (b, head 0, split)
+        const size_t row0 = (size_t)(c + sg.b) * p.H;  // (partial, head 0)
+        const int nh = min(32, p.H - hb);                // this group's heads present
 #pragma unroll 1
         for (int q = 0; q < 4; ++q) {
           uint32_t oa[32];
           tc::tmem_ld32(o_t + 64 * q, oa);
           tc::tmem_wait_ld();
-          const int d = 128 * q + r;
+          // column 128q + r of heads hb.., one 2 KB row apart
+          float* dst = p.part_acc + (row0 + hb) * kLD + 128 * q + r;
 #pragma unroll
-          for (int h = 0; h < 32; ++h) {
-            if (hb + h < p.H)
-              p.part_acc[(row0 + (size_t)(hb + h) * p.splits) * kLD + d] = __uint_as_float(oa[h]);
-          }
+          for (int h = 0; h < 32; ++h)
+            if (h < nh) dst[h * kLD] = __uint_as_float(oa[h]);
         }
-        if (t < p.H)
-          *reinterpret_cast<float2*>(p.part_ml + (row0 + (size_t)t * p.splits) * 2) =
-              make_float2(m_own, l_own);
+        if (t < 64) {  // warps 4 and 5, whole warps (the TMEM load is warp-wide)
+          // Every row of L holds the sums; owner t (lane t % 32) takes column t from its own
+          // lane quarter.
+          uint32_t la[32];
+          tc::tmem_ld32(tbase + lane_off + kLColL + (t & ~31), la);
+          tc::tmem_wait_ld();
+          float l = 0.f;
+#pragma unroll
+          for (int h = 0; h < 32; ++h) l = (h == (t & 31)) ? __uint_as_float(la[h]) : l;
+          if (t < p.H)
+            *reinterpret_cast<float2*>(p.part_ml + (row0 + t) * 2) = make_float2(m_own, l);
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->o_free);
       }
+      ++ns;
     }
   }
 
@@ -568,26 +694,31 @@ __global__ void __launch_bounds__(256) latent_combine_kernel(const LatentArgs a)
   const int w = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (w >= a.B * a.H) return;
-  const int b = w / a.H;
-  int kvl = a.kv_len ? a.kv_len[b] : a.Tk;
-  kvl = min(max(kvl, 1), a.Tk);
-  const int n = (kvl + a.chunk - 1) / a.chunk;
-  const size_t base = (size_t)w * a.splits;
-  const float2* ml = reinterpret_cast<const float2*>(a.part_ml) + base;
+  const int b = w / a.H, h = w % a.H;
+  // The partials of sequence b: CTAs c_lo .. c_hi of the split kernel's partition (with
+  // G = min(grid, T) the CTA holding tile x is ceil((x + 1) G / T) - 1), at index c + b.
+  const int64_t P0 = a.seq_tile0[b], P1 = a.seq_tile0[b + 1], T = a.seq_tile0[a.B];
+  const int64_t G = min((int64_t)a.grid, T);
+  const int c_lo = (int)(((P0 + 1) * G - 1) / T);
+  const int c_hi = (int)((P1 * G - 1) / T);
+  const int n = c_hi - c_lo + 1;
+  const size_t row0 = (size_t)(c_lo + b) * a.H + h;  // partial k is row row0 + k H
+  const float2* ml = reinterpret_cast<const float2*>(a.part_ml);
   float m = -INFINITY;
-  for (int s = lane; s < n; s += 32) m = fmaxf(m, ml[s].x);
+  for (int s = lane; s < n; s += 32) m = fmaxf(m, ml[row0 + (size_t)s * a.H].x);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   float l = 0.f;
   float4 acc[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  const float4* src = reinterpret_cast<const float4*>(a.part_acc + base * kLD) + lane;
+  const float4* src = reinterpret_cast<const float4*>(a.part_acc + row0 * kLD) + lane;
+  const size_t stride = (size_t)a.H * (kLD / 4);  // float4s from one partial to the next
   for (int s0 = 0; s0 < n; s0 += 32) {
     // lane t holds the weight of split s0 + t
     float f = 0.f;
     if (s0 + lane < n) {
-      const float2 v = ml[s0 + lane];
+      const float2 v = ml[row0 + (size_t)(s0 + lane) * a.H];
       f = ex2_approx(v.x - m);
       l += f * v.y;
     }
@@ -598,7 +729,7 @@ __global__ void __launch_bounds__(256) latent_combine_kernel(const LatentArgs a)
 #pragma unroll
       for (int u = 0; u < 2; ++u)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) v[u][k] = src[(size_t)(s0 + s + u) * (kLD / 4) + 32 * k];
+        for (int k = 0; k < 4; ++k) v[u][k] = src[(size_t)(s0 + s + u) * stride + 32 * k];
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const float fu = __shfl_sync(0xffffffffu, f, s + u);
@@ -615,7 +746,7 @@ __global__ void __launch_bounds__(256) latent_combine_kernel(const LatentArgs a)
       const float fu = __shfl_sync(0xffffffffu, f, s);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const float4 v = src[(size_t)(s0 + s) * (kLD / 4) + 32 * k];
+        const float4 v = src[(size_t)(s0 + s) * stride + 32 * k];
         acc[k].x = fmaf(fu, v.x, acc[k].x);
         acc[k].y = fmaf(fu, v.y, acc[k].y);
         acc[k].z = fmaf(fu, v.z, acc[k].z);
@@ -751,8 +882,7 @@ cudaError_t launch_latent(const LatentArgs& a, cudaStream_t stream) {
   p.B = a.B;
   p.H = a.H;
   p.Tk = a.Tk;
-  p.chunk = a.chunk;
-  p.splits = a.splits;
+  p.seq_tile0 = a.seq_tile0;
   p.scale_log2 = a.scale_log2;
 
   static int attr_device = -1;
@@ -783,7 +913,7 @@ cudaError_t launch_latent(const LatentArgs& a, cudaStream_t stream) {
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cfg.gridDim = dim3(a.splits, a.B);
+  cfg.gridDim = dim3(a.grid);
   cfg.blockDim = dim3(kLThreads);
   cfg.dynamicSmemBytes = kLSmem;
   e = cudaLaunchKernelEx(&cfg, latent_splitkv_kernel, p);

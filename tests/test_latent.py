@@ -49,7 +49,8 @@ def _oracle(d, rows=None):
     (2, 16, 700, (200, 700)),  # fewer heads than the MMA's 64 columns
     (5, 64, 2000, (1, 2000)),  # one split per sequence on a busy GPU
     (70, 8, 200, (1, 200)),    # more sequences than one projection block (64) holds
-    (1, 8, 8192, None),        # 64 one-tile splits: the combine's weights in two rounds
+    (1, 8, 8192, None),        # 64 tiles over 64 CTAs: the combine's weights in two rounds
+    (300, 4, 128, (1, 128)),   # more sequences than CTAs: each CTA walks several
 ])
 def test_latent_matches_oracle(B, H, Tk, kv):
     d = _case(B, H, Tk, kv, seed=B * 100 + Tk)
