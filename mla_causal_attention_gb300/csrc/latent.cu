@@ -282,10 +282,27 @@ __global__ void __launch_bounds__(kLThreads, 1)
       bool ok = true;
       uint32_t g = 0;  // key tiles issued over the run
       int nseg = 0;    // segments whose Q was issued
+      // Q of sequence bq, once the previous segment's last score MMA has read Q.
+      auto load_q = [&](int bq) -> bool {
+        if (nseg > 0 && !mbar_wait(&bars->q_empty, (nseg - 1) & 1, p.status, abort_flag))
+          return false;
+        mbar_arrive_expect_tx(&bars->q_full, 9 * kLSubQ);
+        for (int s = 0; s < 8; ++s)
+          tma_load_3d_nohint(sQ + s * kLSubQ, &p.tm_q, &bars->q_full, 64 * s, 0, bq);
+        tma_load_3d_nohint(sQ + 8 * kLSubQ, &p.tm_qr, &bars->q_full, 0, 0, bq);
+        ++nseg;
+        return true;
+      };
       while (ok && walk.next(p, sg)) {
         for (int j = 0; j < sg.nt && ok; ++j, ++g) {
           const int jt = sg.j0 + j * kLatTile;
           const uint32_t prev = (g - 1) & 1u;
+          // A later segment's queries go first: Q is free once the previous segment's last
+          // score MMA has run, which is well before its value mixes release the slots.
+          if (j == 0 && pi == 0 && nseg > 0) {
+            ok = load_q(sg.b);
+            if (!ok) break;
+          }
           // Latent columns 0-511: sub-tile s into slot s once the previous tile's value
           // block s / 2 has released it.
           for (int sidx = pi; sidx < kLSlots; sidx += 2) {
@@ -296,18 +313,13 @@ __global__ void __launch_bounds__(kLThreads, 1)
                                jt, sg.b);
           }
           if (!ok) break;
-          if (j == 0 && pi == 0) {
-            // The segment's queries, once the previous segment's last score MMA has read
-            // Q.  They come from the absorb kernel, which may still be running (this grid
-            // can start early; the latent loads above do not depend on it).
-            if (nseg > 0) ok = mbar_wait(&bars->q_empty, (nseg - 1) & 1, p.status, abort_flag);
+          if (j == 0 && pi == 0 && nseg == 0) {
+            // The first segment's queries come from the absorb kernel, which may still be
+            // running (this grid can start early; the latent loads above do not depend on
+            // it).
+            grid_dep_wait();
+            ok = load_q(sg.b);
             if (!ok) break;
-            if (nseg == 0) grid_dep_wait();
-            mbar_arrive_expect_tx(&bars->q_full, 9 * kLSubQ);
-            for (int s = 0; s < 8; ++s)
-              tma_load_3d_nohint(sQ + s * kLSubQ, &p.tm_q, &bars->q_full, 64 * s, 0, sg.b);
-            tma_load_3d_nohint(sQ + 8 * kLSubQ, &p.tm_qr, &bars->q_full, 0, 0, sg.b);
-            ++nseg;
           }
           // Rotary keys into the P buffer once the previous tile's value mixes are done.
           if (pi == 1) {
