@@ -95,8 +95,7 @@ size_t latent_acc_bytes(int B, int H, int grid) {
 }
 size_t latent_workspace(int B, int H, int grid) {
   return kStatusBytes + latent_q_bytes(B, H) + latent_tile0_bytes(B) +
-         latent_ml_bytes(B, H, grid) + latent_acc_bytes(B, H, grid) +
-         r256((size_t)B * H * 512 * 2);
+         latent_ml_bytes(B, H, grid) + latent_acc_bytes(B, H, grid);
 }
 
 // Rotary workspace: rotated queries [B,H,Tq,64] then rotated new rotary keys [B,Tq,64],
@@ -503,8 +502,6 @@ mla_status mla_latent_decode_fwd(const uint16_t* q_nope, const uint16_t* q_pe,
   a.part_ml = reinterpret_cast<float*>(cur);
   cur += latent_ml_bytes(B, H, pl.grid);
   a.part_acc = reinterpret_cast<float*>(cur);
-  cur += latent_acc_bytes(B, H, pl.grid);
-  a.o_lat = reinterpret_cast<uint16_t*>(cur);
   a.B = B; a.H = H; a.Tk = Tk; a.kv_rows = Tk; a.grid = pl.grid;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   return launch_latent(a, static_cast<cudaStream_t>(cuda_stream)) == cudaSuccess ? MLA_OK

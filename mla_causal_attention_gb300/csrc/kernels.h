@@ -144,7 +144,7 @@ bool encode_bf16_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t r
 // [B,H,64], c_kv [B,kv_rows,512], k_pe [B,kv_rows,64], w_kvb [H*256,512]; out [B,H,128].
 // Workspace pieces (device): q_lat bf16 [B,H,512], seq_tile0 int32 [B+1] (the split kernel's
 // partition), part_ml f32 [(grid+B)*H][2], part_acc f32 [(grid+B)*H][512] (partial c + b of
-// CTA c and sequence b, then head), o_lat bf16 [B,H,512].
+// CTA c and sequence b, then head).
 struct LatentArgs {
   const uint16_t* q_nope;
   const uint16_t* q_pe;
@@ -157,7 +157,6 @@ struct LatentArgs {
   int32_t* seq_tile0;
   float* part_ml;
   float* part_acc;
-  uint16_t* o_lat;
   int* status;
   int B, H, Tk, kv_rows, grid;
   float scale_log2;

@@ -14,11 +14,13 @@
 // projections.
 //
 // Kernels:
-//   latent_absorb_kernel   q_lat[b,h] = W_K[h]^T q_nope[b,h]                 (bf16 out)
-//   latent_splitkv_kernel  per (sequence, key split): scores of 128-key tiles for the 64
-//                          heads, online softmax per head, o_lat partials
-//   latent_combine_kernel  merges the splits' (max, sum, o_lat) per (sequence, head)
-//   latent_upproj_kernel   out[b,h] = W_V[h] o_lat[b,h]                     (bf16 out)
+//   latent_absorb_kernel      q_lat[b,h] = W_K[h]^T q_nope[b,h]              (bf16 out)
+//   latent_splitkv_kernel     one CTA per SM over an equal share of all sequences' 128-key
+//                             tiles: scores for the 64 heads, online softmax per head,
+//                             one o_lat partial per sequence it touches
+//   latent_combine_up_kernel  merges the partials of (sequence, head) into o_lat, then
+//                             out[b,h] = W_V[h] o_lat[b,h]                   (bf16 out)
+// Each kernel after the first is a programmatic dependent launch of the one before.
 //
 // The split kernel runs both MMAs transposed, with keys (and latent columns) on the
 // 128 TMEM lanes and the 64 heads as the N dimension:
@@ -635,9 +637,9 @@ constexpr int kPB = 64;            // sequences per projection CTA
 constexpr int kAbN = 128;          // latent columns per absorb CTA
 constexpr int kAbRow = 128 + 8;    // padded bf16 row (128 values) of the absorb operands
 constexpr int kAbsorbSmem = (128 + kPB) * kAbRow * 2;
-constexpr int kUpN = 32;           // output columns per up-projection CTA
+constexpr int kCuB = 32;           // sequences per merge + up-projection CTA
 constexpr int kUpRow = kLD + 8;    // padded bf16 row (512 values)
-constexpr int kUpSmem = (kUpN + kPB) * kUpRow * 2;
+constexpr int kCuSmem = (128 + kCuB) * kUpRow * 2;
 
 // q_lat[b,h,n] = sum_k W_K[h][k][n] q_nope[b,h,k] for one head, a quarter of the 512 latent
 // columns and 64 sequences: [64 x 128] . [128 x 128].  W_K[h] = rows h*256 .. h*256+127 of
@@ -697,16 +699,11 @@ __global__ void __launch_bounds__(256) latent_absorb_kernel(const LatentArgs a) 
   }
 }
 
-// One warp per (b, h): o_lat = sum_s 2^(m_s - m) acc_s / sum_s 2^(m_s - m) l_s over the
-// splits that hold visible keys, written as bf16 (the up-projection's MMA operand type);
-// lane owns columns 4 lane + 128 k, k = 0..3.
-__global__ void __launch_bounds__(256) latent_combine_kernel(const LatentArgs a) {
-  grid_dep_launch();
-  grid_dep_wait();
-  const int w = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (w >= a.B * a.H) return;
-  const int b = w / a.H, h = w % a.H;
+// Merges the split kernel's partials of one (sequence, head) row into bf16 o_lat (the
+// up-projection's MMA operand type): o_lat = sum_s 2^(m_s - m) acc_s / sum_s 2^(m_s - m) l_s
+// over the CTAs that held the sequence's tiles.  One warp; lane owns columns 4 lane + 128 k.
+__device__ __forceinline__ void latent_merge_row(const LatentArgs& a, int b, int h,
+                                                 int lane, uint16_t* dst) {
   // The partials of sequence b: CTAs c_lo .. c_hi of the split kernel's partition (with
   // G = min(grid, T) the CTA holding tile x is ceil((x + 1) G / T) - 1), at index c + b.
   const int64_t P0 = a.seq_tile0[b], P1 = a.seq_tile0[b + 1], T = a.seq_tile0[a.B];
@@ -716,8 +713,11 @@ __global__ void __launch_bounds__(256) latent_combine_kernel(const LatentArgs a)
   const int n = c_hi - c_lo + 1;
   const size_t row0 = (size_t)(c_lo + b) * a.H + h;  // partial k is row row0 + k H
   const float2* ml = reinterpret_cast<const float2*>(a.part_ml);
-  float m = -INFINITY;
-  for (int s = lane; s < n; s += 32) m = fmaxf(m, ml[row0 + (size_t)s * a.H].x);
+  // (max, sum) of partial s0 + lane, read once per pass of 32 partials
+  float2 mine = make_float2(-INFINITY, 0.f);
+  if (lane < n) mine = ml[row0 + (size_t)lane * a.H];
+  float m = mine.x;
+  for (int s = 32 + lane; s < n; s += 32) m = fmaxf(m, ml[row0 + (size_t)s * a.H].x);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   float l = 0.f;
@@ -727,104 +727,95 @@ __global__ void __launch_bounds__(256) latent_combine_kernel(const LatentArgs a)
   const float4* src = reinterpret_cast<const float4*>(a.part_acc + row0 * kLD) + lane;
   const size_t stride = (size_t)a.H * (kLD / 4);  // float4s from one partial to the next
   for (int s0 = 0; s0 < n; s0 += 32) {
-    // lane t holds the weight of split s0 + t
-    float f = 0.f;
-    if (s0 + lane < n) {
-      const float2 v = ml[row0 + (size_t)(s0 + lane) * a.H];
-      f = ex2_approx(v.x - m);
-      l += f * v.y;
-    }
+    // lane t holds the weight of partial s0 + t
+    if (s0 > 0) mine = s0 + lane < n ? ml[row0 + (size_t)(s0 + lane) * a.H]
+                                     : make_float2(-INFINITY, 0.f);
+    const float f = s0 + lane < n ? ex2_approx(mine.x - m) : 0.f;
+    l += f * mine.y;
     const int cnt = min(32, n - s0);
-    int s = 0;
-    for (; s + 2 <= cnt; s += 2) {  // two splits' rows in flight
-      float4 v[2][4];
+    for (int s = 0; s < cnt; s += 4) {  // up to four partials' rows in flight
+      float4 v[4][4];
 #pragma unroll
-      for (int u = 0; u < 2; ++u)
+      for (int u = 0; u < 4; ++u)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) v[u][k] = src[(size_t)(s0 + s + u) * stride + 32 * k];
+        for (int k = 0; k < 4; ++k)
+          v[u][k] = s + u < cnt ? src[(size_t)(s0 + s + u) * stride + 32 * k]
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const float fu = __shfl_sync(0xffffffffu, f, s + u);
+      for (int u = 0; u < 4; ++u) {
+        const float fu = __shfl_sync(0xffffffffu, f, (s + u) & 31);
+        if (s + u < cnt) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          acc[k].x = fmaf(fu, v[u][k].x, acc[k].x);
-          acc[k].y = fmaf(fu, v[u][k].y, acc[k].y);
-          acc[k].z = fmaf(fu, v[u][k].z, acc[k].z);
-          acc[k].w = fmaf(fu, v[u][k].w, acc[k].w);
+          for (int k = 0; k < 4; ++k) {
+            acc[k].x = fmaf(fu, v[u][k].x, acc[k].x);
+            acc[k].y = fmaf(fu, v[u][k].y, acc[k].y);
+            acc[k].z = fmaf(fu, v[u][k].z, acc[k].z);
+            acc[k].w = fmaf(fu, v[u][k].w, acc[k].w);
+          }
         }
-      }
-    }
-    if (s < cnt) {
-      const float fu = __shfl_sync(0xffffffffu, f, s);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float4 v = src[(size_t)(s0 + s) * stride + 32 * k];
-        acc[k].x = fmaf(fu, v.x, acc[k].x);
-        acc[k].y = fmaf(fu, v.y, acc[k].y);
-        acc[k].z = fmaf(fu, v.z, acc[k].z);
-        acc[k].w = fmaf(fu, v.w, acc[k].w);
       }
     }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
   const float inv = l > 0.f ? 1.f / l : 0.f;
-  uint16_t* dst = a.o_lat + (size_t)w * kLD + 4 * lane;
 #pragma unroll
   for (int k = 0; k < 4; ++k)
-    *reinterpret_cast<uint2*>(dst + 128 * k) =
+    *reinterpret_cast<uint2*>(dst + 4 * lane + 128 * k) =
         make_uint2(pack_bf16x2(acc[k].x * inv, acc[k].y * inv),
                    pack_bf16x2(acc[k].z * inv, acc[k].w * inv));
 }
 
-// out[b,h,n] = sum_k W_V[h][n][k] o_lat[b,h,k] for one head, 32 of its 128 output columns
-// and 64 sequences: [64 x 512] . [512 x 32].  W_V[h] = rows h*256+128 .. h*256+255 of
-// kv_b_proj.  The weight slice is staged before waiting for the combine kernel.  Warp w:
-// row tile w % 4, output columns 16 (w / 4) .. +15.
-__global__ void __launch_bounds__(256) latent_upproj_kernel(const LatentArgs a) {
-  extern __shared__ __align__(16) uint8_t up_smem[];
-  uint16_t* sw = reinterpret_cast<uint16_t*>(up_smem);  // W_V slice: 32 rows (n) x 512 (k)
-  uint16_t* so = sw + kUpN * kUpRow;                     // o_lat: 64 rows (b) x 512 (k)
+// out[b,h,n] = sum_k W_V[h][n][k] o_lat[b,h,k] for one head and 32 sequences:
+// [32 x 512] . [512 x 128].  W_V[h] = rows h*256+128 .. h*256+255 of kv_b_proj.  The weight
+// is staged before waiting for the split kernel; each of the 16 warps then merges 2
+// sequences' rows of o_lat into shared memory, and computes output columns 16 (w % 8) ..
+// + 15 of row tile w / 8.
+__global__ void __launch_bounds__(512) latent_combine_up_kernel(const LatentArgs a) {
+  extern __shared__ __align__(16) uint8_t cu_smem[];
+  uint16_t* sw = reinterpret_cast<uint16_t*>(cu_smem);  // W_V[h]: 128 rows (n) x 512 (k)
+  uint16_t* so = sw + 128 * kUpRow;                      // o_lat: 32 rows (b) x 512 (k)
   const int h = blockIdx.x;
-  const int n0 = blockIdx.y * kUpN;
-  const int b0 = blockIdx.z * kPB;
-  const int nb = min(kPB, a.B - b0);
-  for (int i = threadIdx.x; i < kUpN * (kLD / 8); i += blockDim.x) {
+  const int b0 = blockIdx.y * kCuB;
+  const int nb = min(kCuB, a.B - b0);
+  for (int i = threadIdx.x; i < 128 * (kLD / 8); i += blockDim.x) {
     const int r = i / (kLD / 8), c = i % (kLD / 8);
-    cp_async16(sw + r * kUpRow + c * 8,
-               a.w_kvb + ((size_t)h * 256 + 128 + n0 + r) * kLD + c * 8);
+    cp_async16(sw + r * kUpRow + c * 8, a.w_kvb + ((size_t)h * 256 + 128 + r) * kLD + c * 8);
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
   grid_dep_wait();
-  for (int i = threadIdx.x; i < kPB * (kLD / 8); i += blockDim.x) {
-    const int r = i / (kLD / 8), c = i % (kLD / 8);
-    if (r < nb)
-      cp_async16(so + r * kUpRow + c * 8, a.o_lat + ((size_t)(b0 + r) * a.H + h) * kLD + c * 8);
-    else
-      *reinterpret_cast<uint4*>(so + r * kUpRow + c * 8) = make_uint4(0u, 0u, 0u, 0u);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = warp; i < kCuB; i += 16) {
+    uint16_t* row = so + i * kUpRow;
+    if (i < nb) {
+      latent_merge_row(a, b0 + i, h, lane, row);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        *reinterpret_cast<uint2*>(row + 4 * lane + 128 * k) = make_uint2(0u, 0u);
+    }
   }
   cp_async_wait_all();
   __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int mt = warp & 3, nq = warp >> 2;
   const int g = lane >> 2, c2 = (lane & 3) * 2;
-  float acc[2][4];
+  const int mt = warp >> 3, nw = warp & 7;
+  float acc[2][4];  // [column tile]
 #pragma unroll
   for (int n = 0; n < 2; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-#pragma unroll 8
+#pragma unroll 4
   for (int k0 = 0; k0 < kLD; k0 += 16) {
     uint32_t af[4], bf[4];
     ldsm4(af, so + (mt * 16 + (lane & 15)) * kUpRow + k0 + (lane >> 4) * 8);
     // W_V rows are n with k contiguous (B column-major): matrices (n 0-7, k0), (n 0-7,
     // k0+8), (n 8-15, k0), (n 8-15, k0+8)
-    ldsm4(bf, sw + (nq * 16 + (lane & 7) + ((lane >> 4) << 3)) * kUpRow + k0 +
+    ldsm4(bf, sw + (nw * 16 + (lane & 7) + ((lane >> 4) << 3)) * kUpRow + k0 +
                    ((lane >> 3) & 1) * 8);
     mma16816(acc[0], af, bf[0], bf[1]);
     mma16816(acc[1], af, bf[2], bf[3]);
   }
 #pragma unroll
   for (int n = 0; n < 2; ++n) {
-    const int col = n0 + nq * 16 + n * 8 + c2;
+    const int col = nw * 16 + n * 8 + c2;
     const int r = mt * 16 + g;
     if (r < nb)
       *reinterpret_cast<uint32_t*>(a.out + ((size_t)(b0 + r) * a.H + h) * 128 + col) =
@@ -905,8 +896,8 @@ cudaError_t launch_latent(const LatentArgs& a, cudaStream_t stream) {
     e = cudaFuncSetAttribute(latent_splitkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kLSmem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(latent_upproj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kUpSmem);
+    e = cudaFuncSetAttribute(latent_combine_up_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kCuSmem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(latent_absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kAbsorbSmem);
@@ -930,14 +921,10 @@ cudaError_t launch_latent(const LatentArgs& a, cudaStream_t stream) {
   cfg.dynamicSmemBytes = kLSmem;
   e = cudaLaunchKernelEx(&cfg, latent_splitkv_kernel, p);
   if (e != cudaSuccess) return e;
-  cfg.gridDim = dim3((unsigned)((a.B * a.H + 7) / 8));
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = 0;
-  e = cudaLaunchKernelEx(&cfg, latent_combine_kernel, a);
-  if (e != cudaSuccess) return e;
-  cfg.gridDim = dim3(a.H, 128 / kUpN, bgroups);
-  cfg.dynamicSmemBytes = kUpSmem;
-  e = cudaLaunchKernelEx(&cfg, latent_upproj_kernel, a);
+  cfg.gridDim = dim3(a.H, (unsigned)((a.B + kCuB - 1) / kCuB));
+  cfg.blockDim = dim3(512);
+  cfg.dynamicSmemBytes = kCuSmem;
+  e = cudaLaunchKernelEx(&cfg, latent_combine_up_kernel, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
