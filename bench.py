@@ -354,9 +354,11 @@ def measure_latent(name, args, rank, world, local, with_cpu):
            "ms_per_step": ms, "step_ms_min": min(step_ms), "step_ms_max": max(step_ms),
            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                         "frac": achieved / peak, "traffic": recorded_traffic("latent_splitkv_kernel", name),
-                        "peak_source": peak_src, "kernel": "latent path (4 kernels)",
+                        "peak_source": peak_src,
+                        "kernel": "latent path (3 kernels: absorb, split, merge + "
+                                  "up-projection); traffic is the split kernel's",
                         "algorithmic_per_launch": work},
-           "clocks": clk.summary(), "gpu_launches": 4 * args.steps,
+           "clocks": clk.summary(), "gpu_launches": 3 * args.steps,
            "config": {"workload": name, "B": wl.B, "H": wl.H, "Tk": wl.Tk,
                       "kv_len_range": wl.kv_len_range, "latent": 512, "rope": 64,
                       "weights": "synthetic kv_b_proj ~ N(0, 1/512)",
