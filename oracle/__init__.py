@@ -5,4 +5,4 @@ benchmark use it to check and time the CUDA library.  The library never imports 
 """
 from .oracle import (build_oracle, oracle_rows, oracle_full, oracle_rows_rope,  # noqa: F401
                      round_bf16, library_path, rotate, yarn,
-                     oracle_latent_rows)
+                     oracle_latent_rows, oracle_oproj_rows)

@@ -471,3 +471,80 @@ int mla_oracle_rotate(const uint16_t* x, const int64_t* pos, int64_t n, const do
 
 /* Exposed for the test that pins the diagnostic rounding against torch's own cast. */
 double mla_oracle_round_bf16(double x) { return round_bf16(x); }
+
+/*
+ * Output projection of the attention output.  The MLA init excerpt on "Kimi K2 ·
+ * Similarities" (section "Scale scores") defines o_proj as a linear map from
+ * num_heads x v_head_dim to hidden_size, with bias = attention_bias (false in the
+ * config.json excerpt on "Kimi K2 · Logits"): y = W x, W [N][K] as nn.Linear stores it.
+ * Its input row for (b, i) is the heads' outputs concatenated in head order, feature
+ * k = h * 128 + d of attn [B][H][T][128] (the reshape before o_proj is not shown on the
+ * pages; this is the plain reading).  Sums in fp64 over exact bf16 products.
+ * rows: flat indices b * T + i, or NULL for all B * T rows; out [n_rows][N].
+ */
+typedef struct {
+  const uint16_t* attn;
+  const uint16_t* w;
+  int64_t B, H, T, N, K;
+  const int64_t* rows;
+  int64_t n_rows;
+  double* out;
+  int64_t next;
+  pthread_mutex_t lock;
+} oproj_job_t;
+
+static void* oproj_worker(void* arg) {
+  oproj_job_t* J = (oproj_job_t*)arg;
+  double* x = (double*)malloc((size_t)J->K * sizeof(double));
+  if (!x) return NULL;
+  for (;;) {
+    pthread_mutex_lock(&J->lock);
+    const int64_t r = J->next++;
+    pthread_mutex_unlock(&J->lock);
+    if (r >= J->n_rows) break;
+    const int64_t flat = J->rows ? J->rows[r] : r;
+    const int64_t b = flat / J->T, i = flat % J->T;
+    for (int64_t h = 0; h < J->H; ++h) { /* concatenated head outputs */
+      const uint16_t* src = J->attn + ((b * J->H + h) * J->T + i) * D_V;
+      for (int64_t d = 0; d < D_V; ++d) x[h * D_V + d] = bf16_to_double(src[d]);
+    }
+    double* y = J->out + r * J->N;
+    for (int64_t n = 0; n < J->N; ++n) {
+      const uint16_t* wr = J->w + n * J->K; /* row n of the weight */
+      double acc = 0.0;
+      for (int64_t k = 0; k < J->K; ++k) acc += bf16_to_double(wr[k]) * x[k];
+      y[n] = acc;
+    }
+  }
+  free(x);
+  return NULL;
+}
+
+int mla_oracle_oproj_rows(const uint16_t* attn, const uint16_t* w, int64_t B, int64_t H,
+                          int64_t T, int64_t N, const int64_t* rows, int64_t n_rows,
+                          int nthreads, double* out) {
+  if (!attn || !w || !out) return 11;
+  if (B < 1 || H < 1 || T < 1 || N < 1) return 10;
+  if (rows) {
+    for (int64_t r = 0; r < n_rows; ++r)
+      if (rows[r] < 0 || rows[r] >= B * T) return 13;
+  } else {
+    n_rows = B * T;
+  }
+  oproj_job_t J;
+  memset(&J, 0, sizeof J);
+  J.attn = attn; J.w = w;
+  J.B = B; J.H = H; J.T = T; J.N = N; J.K = H * D_V;
+  J.rows = rows; J.n_rows = n_rows; J.out = out;
+  pthread_mutex_init(&J.lock, NULL);
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 256) nthreads = 256;
+  pthread_t th[256];
+  int started = 0;
+  for (int t = 0; t < nthreads; ++t)
+    if (pthread_create(&th[t], NULL, oproj_worker, &J) == 0) ++started;
+  if (started == 0) oproj_worker(&J);
+  for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
+  pthread_mutex_destroy(&J.lock);
+  return 0;
+}

@@ -76,6 +76,9 @@ def _load():
             lib.mla_oracle_yarn.argtypes = [d, d, d, d, d, d, d, p, p]
             lib.mla_oracle_rotate.restype = ctypes.c_int
             lib.mla_oracle_rotate.argtypes = [p, p, i64, p, d, p]
+            lib.mla_oracle_oproj_rows.restype = ctypes.c_int
+            lib.mla_oracle_oproj_rows.argtypes = [p, p, i64, i64, i64, i64, p, i64,
+                                                  ctypes.c_int, p]
             _lib = lib
     return _lib
 
@@ -242,4 +245,31 @@ def oracle_rows_rope(q_nope, q_pe_raw, k_nope, k_pe, v, kv_len, past_len: int,
                                   _threads(threads), ptr(out), ptr(f), float(mscale))
     if rc != 0:
         raise ValueError(f"oracle rejected its arguments (code {rc})")
+    return out
+
+
+def oracle_oproj_rows(attn, w, rows=None, threads: int | None = None):
+    """Output projection (o_proj) of attention output rows, fp64.
+
+    attn [B,H,T,128] bf16 (the attention core's output), w [N, H*128] bf16 (nn.Linear
+    weight, out_features x in_features).  Row r is (b, i) = divmod(rows[r], T), its input
+    the heads' outputs concatenated in head order.  Returns [n_rows, N].
+    """
+    lib = _load()
+    a, wb = _bits(attn), _bits(w)
+    B, H, T, dv = a.shape
+    N, K = wb.shape
+    assert dv == 128 and K == H * 128
+    if rows is None:
+        rows_arr, n_rows, rows_p = None, B * T, None
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        n_rows, rows_p = rows_arr.size, rows_arr.ctypes.data_as(ctypes.c_void_p)
+    out = np.empty((n_rows, N), dtype=np.float64)
+    rc = lib.mla_oracle_oproj_rows(a.ctypes.data_as(ctypes.c_void_p),
+                                   wb.ctypes.data_as(ctypes.c_void_p), B, H, T, N, rows_p,
+                                   n_rows, _threads(threads),
+                                   out.ctypes.data_as(ctypes.c_void_p))
+    if rc != 0:
+        raise ValueError(f"mla_oracle_oproj_rows failed with code {rc}")
     return out

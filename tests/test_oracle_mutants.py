@@ -66,6 +66,18 @@ LATENT_MUTANTS = {
                             "acc += 0.0; /* shared rotary key */"),
 }
 
+# Mistakes in the output projection, checked against its pins.
+OPROJ_MUTANTS = {
+    "oproj_weight_transposed": ("const uint16_t* wr = J->w + n * J->K; /* row n of the weight */",
+                                "const uint16_t* wr = J->w + n; /* row n of the weight */"),
+    "oproj_head_order": ("for (int64_t d = 0; d < D_V; ++d) x[h * D_V + d] = bf16_to_double(src[d]);",
+                         "for (int64_t d = 0; d < D_V; ++d) x[d * J->H + h] = bf16_to_double(src[d]);"),
+    "oproj_time_ignored": ("const uint16_t* src = J->attn + ((b * J->H + h) * J->T + i) * D_V;",
+                           "const uint16_t* src = J->attn + ((b * J->H + h) * J->T) * D_V;"),
+    "oproj_last_head_dropped": ("for (int64_t h = 0; h < J->H; ++h) { /* concatenated head outputs */",
+                                "for (int64_t h = 0; h < J->H; ++h) { if (h == J->H - 1) { for (int64_t d = 0; d < D_V; ++d) x[h * D_V + d] = 0.0; continue; }"),
+}
+
 
 def _run_pins(name, old, new, tmp_path, pin_file):
     src = open(SRC).read()
@@ -104,3 +116,9 @@ def test_mask_pins_kill_mutant(name, tmp_path):
 def test_latent_pins_kill_mutant(name, tmp_path):
     old, new = LATENT_MUTANTS[name]
     _run_pins(name, old, new, tmp_path, "test_oracle_latent.py")
+
+
+@pytest.mark.parametrize("name", sorted(OPROJ_MUTANTS))
+def test_oproj_pins_kill_mutant(name, tmp_path):
+    old, new = OPROJ_MUTANTS[name]
+    _run_pins(name, old, new, tmp_path, "test_oracle_oproj.py")
