@@ -215,6 +215,30 @@ MLA_API mla_status mla_latent_decode_fwd(const uint16_t* q_nope, const uint16_t*
                                          void* cuda_stream);
 
 /*
+ * Output projection (o_proj) of the attention output.  The MLA init excerpt on "Kimi K2 ·
+ * Similarities" (section "Scale scores") ends the attention block with
+ * o_proj = nn.Linear(num_heads * v_head_dim, hidden_size, bias = attention_bias); the
+ * config.json excerpt on "Kimi K2 · Logits" has hidden_size 7168 and attention_bias false.
+ * Reading of its input (the forward's reshape is not shown): the row for (b, i) is the
+ * heads' outputs concatenated in head order, feature k = 128 h + d of attn, which is read in
+ * place in the layout mla_attn_fwd writes.
+ *
+ *   attn [B, H, T, 128]   bf16, device
+ *   w_o  [N, H * 128]     bf16, device (nn.Linear's weight: out_features x in_features)
+ *   y    [B, T, N]        bf16, device, fully overwritten:
+ *   y[b, i, n] = sum over h, d of w_o[n, 128 h + d] * attn[b, h, i, d]  (fp32 accumulation)
+ * N must be a multiple of 32 and every pointer 16-byte aligned.  Workspace:
+ * mla_oproj_workspace_bytes() (the status word), zeroed once.  Errors: MLA_ERR_NULL,
+ * MLA_ERR_SHAPE (a size < 1, N not a multiple of 32, a tensor too large), MLA_ERR_ALIGN,
+ * MLA_ERR_WORKSPACE, MLA_ERR_DEVICE, MLA_ERR_CUDA; a bounded wait that gives up sets
+ * MLA_ERR_TIMEOUT in the status word (mla_attn_get_status).
+ */
+MLA_API size_t mla_oproj_workspace_bytes(void);
+MLA_API mla_status mla_oproj_fwd(const uint16_t* attn, const uint16_t* w_o, int B, int H, int T,
+                                 int N, uint16_t* y, void* workspace, size_t workspace_bytes,
+                                 void* cuda_stream);
+
+/*
  * Rotary embedding.  The attention excerpt on "Kimi K2 · Similarities" rotates the query's
  * and the new keys' rotary parts before the cache update (rotary_emb gives cos and sin for
  * the positions, apply_rotary_pos_emb rotates q_pe and k_pe), and the rope_scaling block of

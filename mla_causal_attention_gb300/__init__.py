@@ -11,7 +11,7 @@ _BINDING_NAMES = ("MlaAttnError", "mla_attn_fwd", "mla_attn_workspace_bytes",
                   "mla_attn_get_status", "library", "Workspace", "MlaStatus", "PreparedCall",
                   "mla_attn_append_fwd", "mla_attn_rope_append_fwd", "mla_rope_table",
                   "mla_rope_frequencies", "RopeConfig", "mla_attn_masked_fwd",
-                  "mla_latent_decode_fwd")
+                  "mla_latent_decode_fwd", "mla_oproj_fwd")
 
 
 def __getattr__(name):

@@ -66,7 +66,8 @@ EXPORTED = ("mla_attn_workspace_bytes", "mla_attn_fwd", "mla_attn_fwd_ex",
             "mla_attn_append_fwd", "mla_rope_frequencies", "mla_rope_table",
             "mla_attn_rope_workspace_bytes", "mla_attn_rope_append_fwd",
             "mla_attn_masked_workspace_bytes", "mla_attn_masked_fwd",
-            "mla_latent_workspace_bytes", "mla_latent_decode_fwd")
+            "mla_latent_workspace_bytes", "mla_latent_decode_fwd",
+            "mla_oproj_workspace_bytes", "mla_oproj_fwd")
 
 
 def library():
@@ -105,6 +106,10 @@ def library():
         lib.mla_latent_workspace_bytes.argtypes = [i, i, i]
         lib.mla_latent_decode_fwd.restype = i
         lib.mla_latent_decode_fwd.argtypes = [p, p, p, p, p, p, i, i, i, f, p, p, sz, p]
+        lib.mla_oproj_workspace_bytes.restype = sz
+        lib.mla_oproj_workspace_bytes.argtypes = []
+        lib.mla_oproj_fwd.restype = i
+        lib.mla_oproj_fwd.argtypes = [p, p, i, i, i, i, p, p, sz, p]
         lib.mla_rope_frequencies.restype = i
         lib.mla_rope_frequencies.argtypes = [ctypes.POINTER(RopeConfig),
                                              ctypes.POINTER(ctypes.c_double),
@@ -348,6 +353,31 @@ def mla_latent_decode_fwd(q_nope, q_pe, c_kv, k_pe, w_kvb, kv_len, softmax_scale
                                        ctypes.c_void_p(s.cuda_stream))
     if rc != 0:
         raise MlaAttnError(rc, "mla_latent_decode_fwd: ")
+    return out
+
+
+def mla_oproj_fwd(attn, w_o, out=None, workspace: "Workspace | None" = None, stream=None):
+    """Output projection: attn [B,H,T,128], w_o [N, H*128] (bf16, device); returns y [B,T,N]
+    with y[b,i] = w_o @ concat_h attn[b,h,i]."""
+    lib = library()
+    dev = attn.device
+    if dev.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    B, H, T = attn.shape[:3]
+    N = w_o.shape[0]
+    bf = torch.bfloat16
+    _check(attn, "attn", bf, (B, H, T, 128), dev)
+    _check(w_o, "w_o", bf, (N, H * 128), dev)
+    if out is None:
+        out = torch.empty((B, T, N), dtype=bf, device=dev)
+    _check(out, "out", bf, (B, T, N), dev)
+    ws = (workspace or _default_workspace(dev)).get(lib.mla_oproj_workspace_bytes())
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        rc = lib.mla_oproj_fwd(_ptr(attn), _ptr(w_o), B, H, T, N, _ptr(out), _ptr(ws),
+                               ws.numel(), ctypes.c_void_p(s.cuda_stream))
+    if rc != 0:
+        raise MlaAttnError(rc, "mla_oproj_fwd: ")
     return out
 
 

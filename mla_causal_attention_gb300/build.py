@@ -17,7 +17,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmla_attn.so")
-SOURCES = ["host.cu", "decode.cu", "prefill.cu", "noalloc.cu", "rope.cu", "mask.cu", "latent.cu"]
+SOURCES = ["host.cu", "decode.cu", "prefill.cu", "noalloc.cu", "rope.cu", "mask.cu", "latent.cu",
+           "oproj.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

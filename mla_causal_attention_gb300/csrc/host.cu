@@ -508,6 +508,31 @@ mla_status mla_latent_decode_fwd(const uint16_t* q_nope, const uint16_t* q_pe,
                                                                                   : MLA_ERR_CUDA;
 }
 
+size_t mla_oproj_workspace_bytes(void) { return kStatusBytes; }
+
+mla_status mla_oproj_fwd(const uint16_t* attn, const uint16_t* w_o, int B, int H, int T, int N,
+                         uint16_t* y, void* workspace, size_t workspace_bytes,
+                         void* cuda_stream) {
+  if (!attn || !w_o || !y) return MLA_ERR_NULL;
+  if (!workspace) return MLA_ERR_WORKSPACE;
+  if (B < 1 || H < 1 || T < 1 || N < 1 || N % 32 != 0) return MLA_ERR_SHAPE;
+  if ((int64_t)B * H * T * 128 > kMaxElems || (int64_t)N * H * 128 > kMaxElems ||
+      (int64_t)B * T * N > kMaxElems || (int64_t)H * 128 * 2 > (int64_t(1) << 30))
+    return MLA_ERR_SHAPE;
+  if (!aligned16(attn) || !aligned16(w_o) || !aligned16(y) || !aligned16(workspace))
+    return MLA_ERR_ALIGN;
+  if (workspace_bytes < kStatusBytes) return MLA_ERR_WORKSPACE;
+  int sms = 0;
+  mla_status st = check_device(&sms);
+  if (st != MLA_OK) return st;
+  OprojArgs a{};
+  a.attn = attn; a.w = w_o; a.y = y;
+  a.status = static_cast<int*>(workspace);
+  a.B = B; a.H = H; a.T = T; a.N = N;
+  return launch_oproj(a, static_cast<cudaStream_t>(cuda_stream)) == cudaSuccess ? MLA_OK
+                                                                                : MLA_ERR_CUDA;
+}
+
 mla_status mla_attn_fwd(const uint16_t* q_nope, const uint16_t* q_pe, const uint16_t* k_nope,
                         const uint16_t* k_pe_shared, const uint16_t* v, const int32_t* kv_len,
                         int B, int H, int Tq, int Tk, int past_len, float softmax_scale,

@@ -140,6 +140,22 @@ cudaError_t launch_masked_rows_fixup(const FixupArgs& a, cudaStream_t stream);
 bool encode_bf16_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
                     uint64_t planes, uint64_t plane_rows, uint32_t box_rows);
 
+// bf16 tensor map of any rank (<= 5) with 128-byte swizzled boxes; dims innermost first,
+// strides_bytes for dims 1.. (rank - 1 entries); elements past dims read as zeros.
+bool encode_bf16_tiled(CUtensorMap* m, const void* base, int rank, const uint64_t* dims,
+                       const uint64_t* strides_bytes, const uint32_t* box);
+
+// Output projection (o_proj) of the attention output: y [B,T,N] = W [N,H*128] applied to
+// each (b, i) row of attn [B,H,T,128] with the heads concatenated in head order.
+struct OprojArgs {
+  const uint16_t* attn;
+  const uint16_t* w;
+  uint16_t* y;
+  int* status;
+  int B, H, T, N;
+};
+cudaError_t launch_oproj(const OprojArgs& a, cudaStream_t stream);
+
 // Decode over the latent cache (absorbed kv_b_proj).  Shapes: q_nope [B,H,128], q_pe
 // [B,H,64], c_kv [B,kv_rows,512], k_pe [B,kv_rows,64], w_kvb [H*256,512]; out [B,H,128].
 // Workspace pieces (device): q_lat bf16 [B,H,512], seq_tile0 int32 [B+1] (the split kernel's

@@ -1,0 +1,309 @@
+// oproj.cu -- the output projection (o_proj) after the attention core, on sm_103a tensor
+// cores.
+//
+// The MLA init excerpt on "Kimi K2 · Similarities" (section "Scale scores") ends the attention
+// block with o_proj, a linear map from num_heads x v_head_dim = 64 x 128 to hidden_size (7168
+// and no bias in the config.json excerpt on "Kimi K2 · Logits").  Its input row for (b, i) is
+// the heads' outputs concatenated in head order, so
+//   y[b, i, n] = sum_{h, d} W[n, 128 h + d] attn[b, h, i, d]
+// a GEMM with M = B * T rows, K = 128 H, N outputs.  It reads the attention output where the
+// attention core left it ([B, H, T, 128]) through a 4-D tensor map: a 64-column slice of K is
+// half of one head, and a 128-row box is 128 positions of one sequence (T > 1) or 128
+// sequences (T = 1, decode).
+//
+// One CTA per 128-row x BN-column output tile (BN = 256, or 64 when there are few row tiles,
+// so that more SMs share the weight), 256 threads:
+//   warps 0, 2, 3  TMA producers (the A slice; the two halves of the weight slice: one
+//                  thread's TMA issue rate is below what this loop consumes);
+//   warp 1         allocates the TMEM accumulator, issues M128 x BN x K16 MMAs (A and B
+//                  both K-major from 128-byte swizzled shared memory);
+//   warps 4-7      epilogue: TMEM -> registers -> bf16 -> global, one row per thread.
+#include <cuda.h>
+
+#include <algorithm>
+#include <atomic>
+#include <mutex>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "tcgen05.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kOpBM = 128;      // rows per tile (TMEM lanes)
+constexpr int kOpBK = 64;       // K per stage: one 128-byte swizzled row of bf16
+constexpr int kOpASub = kOpBM * kOpBK * 2;  // 16 KB
+
+template <int BN>
+struct OpCfg {
+  static constexpr int kBBytes = BN * kOpBK * 2;               // weight slice
+  static constexpr int kStage = kOpASub + kBBytes;
+  static constexpr int kStages = BN == 256 ? 4 : 8;
+  static constexpr int kBarOff = kStages * kStage;
+  static constexpr int kSmem = kBarOff + 256 + 1024;
+  static constexpr int kBoxN = BN > 128 ? 128 : BN;            // rows per weight box
+  static constexpr int kWProd = BN / kBoxN;                    // weight producers
+  static_assert(kSmem <= 232448, "shared memory per block");
+};
+
+struct OprojParams {
+  CUtensorMap tm_a;  // attn {128, T, H, B}
+  CUtensorMap tm_w;  // w {K, N}
+  uint16_t* y;
+  int* status;
+  int B, H, T, N, K;
+  int m_tiles_per_b;  // T > 1: row tiles per sequence; T == 1: 0
+};
+
+struct OpBars {
+  uint64_t full[8];
+  uint64_t empty[8];
+  uint64_t acc_full;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int BN>
+__global__ void __launch_bounds__(256, 1) oproj_kernel(const __grid_constant__ OprojParams p) {
+  using C = OpCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  OpBars* bars = reinterpret_cast<OpBars*>(smem + C::kBarOff);
+  volatile int* abort_flag = &bars->abort_flag;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int KB = p.K / kOpBK;
+
+  // This tile's rows: (b, i0 .. i0 + 127) for T > 1, sequences b0 .. b0 + 127 for T == 1.
+  const int mt = blockIdx.x;
+  const int n0 = blockIdx.y * BN;
+  int b = 0, i0 = 0;
+  if (p.m_tiles_per_b > 0) {
+    b = mt / p.m_tiles_per_b;
+    i0 = (mt % p.m_tiles_per_b) * kOpBM;
+  } else {
+    b = mt * kOpBM;
+  }
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&bars->full[s], 1 + C::kWProd);  // the A producer and the weight producers
+      mbar_init(&bars->empty[s], 1);
+    }
+    mbar_init(&bars->acc_full, 1);
+    bars->abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(&bars->tmem_base, BN);
+    tc::tmem_relinquish();
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tbase = bars->tmem_base;
+
+  if ((warp == 0 || warp == 2 || warp == 3) && lane == 0) {
+    // ================= TMA producers =================
+    // warp 0: the A slice (16 KB); warps 2 and 3: weight rows n0 .. n0 + 127 and
+    // n0 + 128 .. n0 + 255 (BN = 256; warp 2 alone for BN = 64).
+    const int role = warp == 0 ? 0 : warp - 1;  // 0 = A, 1.. = weight box
+    if (role <= C::kWProd) {
+      prefetch_tmap(role == 0 ? (const void*)&p.tm_a : (const void*)&p.tm_w);
+      int posted = 0;
+      for (int kb = 0; kb < KB; ++kb) {
+        const int s = kb % C::kStages;
+        if (kb >= C::kStages &&
+            !mbar_wait(&bars->empty[s], ((kb / C::kStages) - 1) & 1, p.status, abort_flag))
+          break;
+        uint8_t* stage = smem + s * C::kStage;
+        if (role == 0) {
+          mbar_arrive_expect_tx(&bars->full[s], kOpASub);
+          const int h = kb >> 1, d0 = (kb & 1) * kOpBK;
+          if (p.m_tiles_per_b > 0)
+            tma_load_4d(stage, &p.tm_a, &bars->full[s], d0, i0, h, b);
+          else
+            tma_load_4d(stage, &p.tm_a, &bars->full[s], d0, 0, h, b);
+        } else {
+          mbar_arrive_expect_tx(&bars->full[s], C::kBoxN * kOpBK * 2);
+          const int r = (role - 1) * C::kBoxN;
+          tma_load_2d(stage + kOpASub + r * kOpBK * 2, &p.tm_w, &bars->full[s], kb * kOpBK,
+                      n0 + r);
+        }
+        posted = kb + 1;
+      }
+      // Loads in flight must land before the CTA's shared memory is released.
+      for (int kb = max(0, posted - C::kStages); kb < posted; ++kb) {
+        const uint32_t a = smem_u32(&bars->full[kb % C::kStages]);
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(a, (kb / C::kStages) & 1))
+          if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+      }
+    }
+  } else if (warp == 1) {
+    // ================= MMA issuer =================
+    constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kOpBM, BN, false);
+    const uint64_t dhi = tc::smem_desc_sw128(0, 16, 1024);
+    const uint32_t base_lo = smem_u32(smem) >> 4;
+    bool ok = true;
+    for (int kb = 0; kb < KB && ok; ++kb) {
+      const int s = kb % C::kStages;
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(&bars->full[s], (kb / C::kStages) & 1, p.status, abort_flag));
+      if (!ok) break;
+      tc::fence_after_sync();
+      const uint32_t a_lo = base_lo + (s * C::kStage >> 4);
+      const uint32_t b_lo = a_lo + (kOpASub >> 4);
+      if (tc::elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < kOpBK / 16; ++kk) {
+          const uint32_t koff = kk * (32 >> 4);
+          tc::mma_ss(tbase, dhi | (uint64_t)(a_lo + koff), dhi | (uint64_t)(b_lo + koff), kIdesc,
+                     (kb | kk) != 0 ? 1u : 0u);
+        }
+        tc::commit(&bars->empty[s]);
+      }
+      __syncwarp();
+    }
+    if (tc::elect_one()) tc::commit(&bars->acc_full);  // also after a failed wait: no MMA
+    __syncwarp();                                      // may still run at the dealloc
+  } else if (warp >= 4) {
+    // ================= epilogue =================
+    const int q = warp & 3;
+    const int r = q * 32 + lane;  // tile row = TMEM lane
+    const bool got =
+        __all_sync(0xffffffffu, mbar_wait(&bars->acc_full, 0, p.status, abort_flag));
+    if (got) {
+      tc::fence_after_sync();
+      bool row_ok;
+      size_t row;
+      if (p.m_tiles_per_b > 0) {
+        row_ok = i0 + r < p.T;
+        row = (size_t)b * p.T + i0 + r;
+      } else {
+        row_ok = b + r < p.B;
+        row = (size_t)(b + r);
+      }
+      uint16_t* dst = p.y + row * p.N + n0;
+      const uint32_t t_row = tbase + ((uint32_t)(q * 32) << 16);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t v[32];
+        tc::tmem_ld32(t_row + c * 32, v);
+        tc::tmem_wait_ld();
+        if (row_ok && n0 + c * 32 < p.N) {
+          uint4* o = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(v[8 * u + 0]), __uint_as_float(v[8 * u + 1]));
+            w.y = pack_bf16x2(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3]));
+            w.z = pack_bf16x2(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5]));
+            w.w = pack_bf16x2(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7]));
+            o[u] = w;
+          }
+        }
+      }
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tbase, BN);
+  }
+}
+
+// Tensor maps cached by pointers and sizes (encoding costs microseconds of host time).
+struct OpKey {
+  const void* a;
+  const void* w;
+  int B, H, T, N, bn;
+  bool operator==(const OpKey& o) const {
+    return a == o.a && w == o.w && B == o.B && H == o.H && T == o.T && N == o.N && bn == o.bn;
+  }
+};
+struct OpEntry {
+  OpKey key;
+  CUtensorMap a, w;
+  bool valid;
+};
+std::mutex g_op_mu;
+OpEntry g_op[8];
+int g_op_next = 0;
+
+bool oproj_maps(const OprojArgs& a, int bn, OprojParams* p) {
+  const OpKey key{a.attn, a.w, a.B, a.H, a.T, a.N, bn};
+  std::lock_guard<std::mutex> lk(g_op_mu);
+  for (const OpEntry& e : g_op) {
+    if (e.valid && e.key == key) {
+      p->tm_a = e.a;
+      p->tm_w = e.w;
+      return true;
+    }
+  }
+  const uint64_t dims_a[4] = {128, (uint64_t)a.T, (uint64_t)a.H, (uint64_t)a.B};
+  const uint64_t str_a[3] = {256, (uint64_t)a.T * 256, (uint64_t)a.H * a.T * 256};
+  const uint32_t box_a[4] = {64, a.T > 1 ? 128u : 1u, 1, a.T > 1 ? 1u : 128u};
+  const uint64_t K = (uint64_t)a.H * 128;
+  const uint64_t dims_w[2] = {K, (uint64_t)a.N};
+  const uint64_t str_w[1] = {K * 2};
+  const uint32_t box_w[2] = {64, (uint32_t)std::min(bn, 128)};
+  if (!encode_bf16_tiled(&p->tm_a, a.attn, 4, dims_a, str_a, box_a) ||
+      !encode_bf16_tiled(&p->tm_w, a.w, 2, dims_w, str_w, box_w))
+    return false;
+  OpEntry& e = g_op[g_op_next];
+  g_op_next = (g_op_next + 1) % 8;
+  e.key = key;
+  e.a = p->tm_a;
+  e.w = p->tm_w;
+  e.valid = true;
+  return true;
+}
+
+template <int BN>
+cudaError_t launch_bn(const OprojArgs& a, int m_tiles, cudaStream_t stream) {
+  using C = OpCfg<BN>;
+  OprojParams p;
+  if (!oproj_maps(a, BN, &p)) return cudaErrorInvalidValue;
+  p.y = a.y;
+  p.status = a.status;
+  p.B = a.B;
+  p.H = a.H;
+  p.T = a.T;
+  p.N = a.N;
+  p.K = a.H * 128;
+  p.m_tiles_per_b = a.T > 1 ? (a.T + kOpBM - 1) / kOpBM : 0;
+  static std::atomic<uint64_t> attr_done{0};  // bit per device: smem attribute set
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(attr_done.load() & bit)) {
+    e = cudaFuncSetAttribute(oproj_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmem);
+    if (e != cudaSuccess) return e;
+    attr_done.fetch_or(bit);
+  }
+  const dim3 grid((unsigned)m_tiles, (unsigned)((a.N + BN - 1) / BN));
+  oproj_kernel<BN><<<grid, 256, C::kSmem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_oproj(const OprojArgs& a, cudaStream_t stream) {
+  const int64_t m_tiles = a.T > 1 ? (int64_t)a.B * ((a.T + kOpBM - 1) / kOpBM)
+                                  : ((int64_t)a.B + kOpBM - 1) / kOpBM;
+  if (m_tiles > 0x7fffffff) return cudaErrorInvalidValue;
+  // Few row tiles (decode): narrow column tiles so that more SMs stream the weight.
+  const int sms = device_sm_count();
+  if (m_tiles * ((a.N + 255) / 256) < (sms > 0 ? sms : 152))
+    return launch_bn<64>(a, (int)m_tiles, stream);
+  return launch_bn<256>(a, (int)m_tiles, stream);
+}
+
+}  // namespace mla

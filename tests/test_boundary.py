@@ -138,3 +138,25 @@ def test_masked_entry_host_errors(lib):
         lib.mla_attn_workspace_bytes(3, 8, 1, 300)
     if not torch.cuda.is_available():
         assert call(km) in (S.ERR_CUDA, S.ERR_DEVICE)
+
+
+def test_oproj_host_errors(lib):
+    """mla_oproj_fwd rejects bad arguments before any device work."""
+    buf = ctypes.create_string_buffer(1 << 16)
+    base = (ctypes.addressof(buf) + 255) & ~255
+    p = lambda off=0: ctypes.c_void_p(base + off)  # noqa: E731
+    ws, n = p(), 256
+    assert lib.mla_oproj_workspace_bytes() == 256
+    # null pointers
+    assert lib.mla_oproj_fwd(None, p(), 1, 1, 1, 32, p(), ws, n, None) == binding.MlaStatus.ERR_NULL
+    assert lib.mla_oproj_fwd(p(), p(), 1, 1, 1, 32, None, ws, n, None) == binding.MlaStatus.ERR_NULL
+    # sizes: N a multiple of 32, every size >= 1
+    for B, H, T, N in [(0, 1, 1, 32), (1, 0, 1, 32), (1, 1, 0, 32), (1, 1, 1, 48), (1, 1, 1, 0)]:
+        assert lib.mla_oproj_fwd(p(), p(), B, H, T, N, p(), ws, n, None) == \
+            binding.MlaStatus.ERR_SHAPE, (B, H, T, N)
+    # alignment and workspace
+    assert lib.mla_oproj_fwd(p(8), p(), 1, 1, 1, 32, p(), ws, n, None) == binding.MlaStatus.ERR_ALIGN
+    assert lib.mla_oproj_fwd(p(), p(), 1, 1, 1, 32, p(), None, n, None) == \
+        binding.MlaStatus.ERR_WORKSPACE
+    assert lib.mla_oproj_fwd(p(), p(), 1, 1, 1, 32, p(), ws, 8, None) == \
+        binding.MlaStatus.ERR_WORKSPACE
