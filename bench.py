@@ -48,6 +48,8 @@ def parse_args():
     ap.add_argument("--secondary", default="decode_ragged")
     ap.add_argument("--latent", default="latent_decode_ragged",
                     help="decode over the latent cache, reported under secondary (or none)")
+    ap.add_argument("--oproj", default="oproj_long_prefill",
+                    help="output projection workload, reported under secondary (or none)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
@@ -387,6 +389,104 @@ def measure_latent(name, args, rank, world, local, with_cpu):
     return res
 
 
+OPROJ_WORKLOADS = {
+    # the long prefill's attention output projected (rows = 4096 positions)
+    "oproj_long_prefill": dict(B=1, H=64, T=4096, N=7168),
+    # the ragged decode batch's outputs projected (rows = 64 sequences)
+    "oproj_decode_b64": dict(B=64, H=64, T=1, N=7168),
+}
+
+
+def measure_oproj(name, args, rank, world, local, with_cpu):
+    """Output projection (o_proj): TFLOP/s for the prefill shape, GB/s for the decode shape."""
+    import ctypes
+
+    import numpy as np
+    import torch
+
+    from mla_causal_attention_gb300 import binding
+    from mla_causal_attention_gb300.inputs import make_oproj_inputs
+
+    c = OPROJ_WORKLOADS[name]
+    B, H, T, N = c["B"], c["H"], c["T"], c["N"]
+    K = H * 128
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    host = make_oproj_inputs(B, H, T, N, seed=args.seed + rank)
+    attn, w = host["attn"].to(dev), host["w_o"].to(dev)
+    y = torch.empty((B, T, N), dtype=torch.bfloat16, device=dev)
+    lib = binding.library()
+    wsobj = binding.Workspace(dev)
+    ws = wsobj.get(lib.mla_oproj_workspace_bytes())
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    tensor_bound = T > 1
+    flops = 2.0 * B * T * K * N
+    bytes_ = (B * T * K + N * K + B * T * N) * 2
+    work = flops if tensor_bound else bytes_
+    P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    cargs = (P(attn), P(w), B, H, T, N, P(y), P(ws), ctypes.c_size_t(ws.numel()),
+             ctypes.c_void_p(stream.cuda_stream))
+
+    def call():
+        rc = lib.mla_oproj_fwd(*cargs)
+        if rc != 0:
+            raise RuntimeError(f"mla_oproj_fwd returned {rc}")
+
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            starts[i].record(stream)
+            call()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = max_over_ranks(sum(step_ms), world, dev) / args.steps
+    if binding.mla_attn_get_status(wsobj, dev) != 0:
+        raise RuntimeError("device status set by the output projection")
+    unit_scale, unit = (1e-12, "TFLOP/s") if tensor_bound else (1e-9, "GB/s")
+    peak, peak_src = peak_for("tensor" if tensor_bound else "hbm", False)
+    achieved = work / (ms * 1e-3) * unit_scale
+    res = {"workload": name, "value": whole_job_rate(work, world, ms, unit_scale), "unit": unit,
+           "ms_per_step": ms, "step_ms_min": min(step_ms), "step_ms_max": max(step_ms),
+           "roofline": {"bound": "tensor" if tensor_bound else "hbm", "achieved": achieved,
+                        "peak": peak, "unit": unit, "frac": achieved / peak,
+                        "traffic": recorded_traffic("oproj_kernel", name),
+                        "peak_source": peak_src, "kernel": "oproj_kernel",
+                        "algorithmic_per_launch": work},
+           "clocks": clk.summary(), "gpu_launches": args.steps,
+           "config": {"workload": name, "B": B, "H": H, "T": T, "in_features": K,
+                      "out_features": N, "weights": "synthetic o_proj ~ N(0, 1/8192)",
+                      "l2": "flushed (2x L2 write) before every timed step, outside its events"}}
+    if with_cpu and rank == 0 and world == 1:
+        from oracle import oracle_oproj_rows
+
+        rng = np.random.default_rng(args.seed)
+        t0 = time.perf_counter()
+        rows = []
+        while time.perf_counter() - t0 < min(args.cpu_seconds, 5.0):
+            r = [int(x) for x in rng.integers(0, B * T, 16)]
+            oracle_oproj_rows(host["attn"], host["w_o"], rows=r)
+            rows += r
+        dt = time.perf_counter() - t0
+        # the sample's share of the problem's algorithmic work
+        cpu_work = work * len(rows) / (B * T)
+        res["cpu_baseline"] = {"value": cpu_work / dt * unit_scale, "unit": unit,
+                               "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+                               "sample": f"{len(rows)} random output rows, {dt:.1f} s",
+                               "seconds": dt}
+    del flush
+    return res
+
+
 def measure_e2e(wl, host, d, out, ws, stream, m, args, world):
     """Same metric through the public API from pinned host memory, copies included."""
     import torch
@@ -567,6 +667,9 @@ def main():
     lat = None
     if args.latent and args.latent != "none":
         lat = measure_latent(args.latent, args, rank, world, local, with_cpu=not args.no_cpu)
+    opj = None
+    if args.oproj and args.oproj != "none":
+        opj = measure_oproj(args.oproj, args, rank, world, local, with_cpu=not args.no_cpu)
     if rank == 0:
         m = workload_metrics(wl, [wl.Tk] * wl.B)
         line = base_line(args, wl, m, res["value"], res["ms_per_step"])
@@ -581,6 +684,8 @@ def main():
                                                                 if k != "work_per_step"}}]
         if lat is not None:
             line.setdefault("secondary", []).append(lat)
+        if opj is not None:
+            line.setdefault("secondary", []).append(opj)
         print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()

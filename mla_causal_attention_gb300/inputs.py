@@ -21,7 +21,7 @@ import torch
 from .workloads import Workload
 
 _TENSOR_IDS = {"q_nope": 1, "q_pe": 2, "k_nope": 3, "k_pe_shared": 4, "v": 5, "kv_len": 6,
-               "c_kv": 7, "w_kvb": 8}
+               "c_kv": 7, "w_kvb": 8, "attn": 9, "w_o": 10}
 _MASK64 = (1 << 64) - 1
 
 
@@ -121,4 +121,20 @@ def make_latent_inputs(wl: Workload, seed: int = 0, pin_memory: bool = False) ->
     t["kv_len"] = draw_kv_len(wl, seed)
     if pin_memory:
         t["kv_len"] = t["kv_len"].pin_memory()
+    return t
+
+
+def make_oproj_inputs(B: int, H: int, T: int, N: int, seed: int = 0) -> dict:
+    """Inputs of the output projection: attn [B,H,T,128] ~ N(0,1) (an attention output's
+    shape) and the o_proj weight w_o [N, H*128] ~ N(0, 1/(H*128)), so outputs are ~N(0,1)
+    (synthetic: no trained weights)."""
+    t = {"attn": torch.empty((B, H, T, 128), dtype=torch.bfloat16),
+         "w_o": torch.empty((N, H * 128), dtype=torch.bfloat16)}
+    jobs = [(t["attn"][b, h], "attn", b, h, 1.0) for b in range(B) for h in range(H)]
+    rows = 256  # weight chunks of 256 output rows
+    jobs += [(t["w_o"][r:r + rows], "w_o", 0, r // rows, (H * 128) ** -0.5)
+             for r in range(0, N, rows)]
+    threads = min(32, os.cpu_count() or 1)
+    with ThreadPoolExecutor(threads) as ex:
+        list(ex.map(lambda j: _draw(j[0], seed, j[1], j[2], j[3], j[4]), jobs))
     return t
