@@ -11,10 +11,9 @@
 // half of one head, and a 128-row box is 128 positions of one sequence (T > 1) or 128
 // sequences (T = 1, decode).
 //
-// One CTA per 128-row x BN-column output tile (BN = 256, or 64 when there are few row tiles,
-// so that more SMs share the weight), 256 threads:
-//   warps 0, 2, 3  TMA producers (the A slice; the two halves of the weight slice: one
-//                  thread's TMA issue rate is below what this loop consumes);
+// One CTA per 128-row x BN-column output tile (BN = 256; with few row tiles, as in decode,
+// 48 or 64 so that about one CTA per SM streams its share of the weight), 256 threads:
+//   warps 0, 2, 3  TMA producers (the A slice; the two halves of the weight slice);
 //   warp 1         allocates the TMEM accumulator, issues M128 x BN x K16 MMAs (A and B
 //                  both K-major from 128-byte swizzled shared memory);
 //   warps 4-7      epilogue: TMEM -> registers -> bf16 -> global, one row per thread.
@@ -40,6 +39,8 @@ struct OpCfg {
   static constexpr int kBBytes = BN * kOpBK * 2;               // weight slice
   static constexpr int kStage = kOpASub + kBBytes;
   static constexpr int kStages = BN == 256 ? 4 : 8;
+  static constexpr int kTmemCols = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
+  static_assert(kStage % 1024 == 0 && BN % 16 == 0, "stage alignment, MMA N");
   static constexpr int kBarOff = kStages * kStage;
   static constexpr int kSmem = kBarOff + 256 + 1024;
   static constexpr int kBoxN = BN > 128 ? 128 : BN;            // rows per weight box
@@ -97,7 +98,7 @@ __global__ void __launch_bounds__(256, 1) oproj_kernel(const __grid_constant__ O
     fence_barrier_init();
   }
   if (warp == 1) {
-    tc::tmem_alloc(&bars->tmem_base, BN);
+    tc::tmem_alloc(&bars->tmem_base, C::kTmemCols);
     tc::tmem_relinquish();
   }
   tc::fence_before_sync();
@@ -108,7 +109,7 @@ __global__ void __launch_bounds__(256, 1) oproj_kernel(const __grid_constant__ O
   if ((warp == 0 || warp == 2 || warp == 3) && lane == 0) {
     // ================= TMA producers =================
     // warp 0: the A slice (16 KB); warps 2 and 3: weight rows n0 .. n0 + 127 and
-    // n0 + 128 .. n0 + 255 (BN = 256; warp 2 alone for BN = 64).
+    // n0 + 128 .. n0 + 255 (BN = 256; warp 2 alone for narrower tiles).
     const int role = warp == 0 ? 0 : warp - 1;  // 0 = A, 1.. = weight box
     if (role <= C::kWProd) {
       prefetch_tmap(role == 0 ? (const void*)&p.tm_a : (const void*)&p.tm_w);
@@ -189,14 +190,14 @@ __global__ void __launch_bounds__(256, 1) oproj_kernel(const __grid_constant__ O
       uint16_t* dst = p.y + row * p.N + n0;
       const uint32_t t_row = tbase + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t v[32];
-        tc::tmem_ld32(t_row + c * 32, v);
+      for (int c = 0; c < BN / 16; ++c) {
+        uint32_t v[16];
+        tc::tmem_ld16(t_row + c * 16, v);
         tc::tmem_wait_ld();
-        if (row_ok && n0 + c * 32 < p.N) {
-          uint4* o = reinterpret_cast<uint4*>(dst + c * 32);
+        if (row_ok && n0 + c * 16 < p.N) {
+          uint4* o = reinterpret_cast<uint4*>(dst + c * 16);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
+          for (int u = 0; u < 2; ++u) {
             uint4 w;
             w.x = pack_bf16x2(__uint_as_float(v[8 * u + 0]), __uint_as_float(v[8 * u + 1]));
             w.y = pack_bf16x2(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3]));
@@ -213,7 +214,7 @@ __global__ void __launch_bounds__(256, 1) oproj_kernel(const __grid_constant__ O
   __syncthreads();
   if (warp == 1) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tbase, BN);
+    tc::tmem_dealloc(tbase, C::kTmemCols);
   }
 }
 
@@ -299,10 +300,13 @@ cudaError_t launch_oproj(const OprojArgs& a, cudaStream_t stream) {
   const int64_t m_tiles = a.T > 1 ? (int64_t)a.B * ((a.T + kOpBM - 1) / kOpBM)
                                   : ((int64_t)a.B + kOpBM - 1) / kOpBM;
   if (m_tiles > 0x7fffffff) return cudaErrorInvalidValue;
-  // Few row tiles (decode): narrow column tiles so that more SMs stream the weight.
-  const int sms = device_sm_count();
-  if (m_tiles * ((a.N + 255) / 256) < (sms > 0 ? sms : 152))
+  // Few row tiles (decode): narrow column tiles so that about one CTA per SM streams its
+  // share of the weight (48 columns: 150 tiles of a 7168-wide weight on 152 SMs).
+  const int sms = device_sm_count() > 0 ? device_sm_count() : 152;
+  if (m_tiles * ((a.N + 255) / 256) < sms) {
+    if (m_tiles * ((a.N + 47) / 48) <= sms) return launch_bn<48>(a, (int)m_tiles, stream);
     return launch_bn<64>(a, (int)m_tiles, stream);
+  }
   return launch_bn<256>(a, (int)m_tiles, stream);
 }
 

@@ -3,9 +3,10 @@
 o_proj maps the 64 heads' concatenated 128-wide outputs to hidden_size (the MLA init excerpt
 on "Kimi K2 · Similarities", section "Scale scores"; 7168, no bias, in the config.json excerpt
 on "Kimi K2 · Logits").  The kernel reads the attention output in place ([B,H,T,128]).
-Cases: ragged row tiles (T not a multiple of 128), N not a multiple of the 256-column tile,
-decode rows (T = 1, more and fewer than 128 sequences), the model's widths sampled, and the
-attention output of the library itself fed through.
+Cases: ragged row tiles (T not a multiple of 128), N not a multiple of the column tile,
+decode rows (T = 1, more and fewer than 128 sequences), each column-tile width (48, 64,
+256), the model's widths sampled, and the attention output of the library itself fed
+through.
 """
 import numpy as np
 import pytest
@@ -62,6 +63,14 @@ def test_oproj_kimi_widths_decode_sampled():
     rng = np.random.default_rng(1)
     rows = sorted({0, 63, *rng.integers(0, B, 6).tolist()})
     _check(B, H, T, N, seed=3, rows=rows, label="oproj decode widths")
+
+
+def test_oproj_two_decode_row_tiles_model_width_sampled():
+    """130 sequences: two row tiles at the 7168 width take the 64-column tile path."""
+    B, H, T, N = 130, 16, 1, 7168
+    rng = np.random.default_rng(6)
+    rows = sorted({0, 127, 128, 129, *rng.integers(0, B, 6).tolist()})
+    _check(B, H, T, N, seed=6, rows=rows, label="oproj 64-column tiles")
 
 
 def test_oproj_kimi_widths_prefill_sampled():
