@@ -11,8 +11,10 @@
 // half of one head, and a 128-row box is 128 positions of one sequence (T > 1) or 128
 // sequences (T = 1, decode).
 //
-// One CTA per 128-row x BN-column output tile (BN = 256; with few row tiles, as in decode,
-// 48 or 64 so that about one CTA per SM streams its share of the weight), 256 threads:
+// Persistent: one CTA per SM walks 128-row x BN-column output tiles (BN = 256; with few row
+// tiles, as in decode, 48 or 64 so that about one CTA per SM streams its share of the
+// weight), with two TMEM accumulators so one tile's epilogue overlaps the next tile's K
+// loop.  256 threads:
 //   warps 0, 2, 3  TMA producers (the A slice; the two halves of the weight slice);
 //   warp 1         allocates the TMEM accumulator, issues M128 x BN x K16 MMAs (A and B
 //                  both K-major from 128-byte swizzled shared memory);
@@ -40,6 +42,7 @@ struct OpCfg {
   static constexpr int kStage = kOpASub + kBBytes;
   static constexpr int kStages = BN == 256 ? 4 : 8;
   static constexpr int kTmemCols = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
+  static_assert(2 * kTmemCols <= 512, "two accumulators in TMEM");
   static_assert(kStage % 1024 == 0 && BN % 16 == 0, "stage alignment, MMA N");
   static constexpr int kBarOff = kStages * kStage;
   static constexpr int kSmem = kBarOff + 256 + 1024;
@@ -55,15 +58,38 @@ struct OprojParams {
   int* status;
   int B, H, T, N, K;
   int m_tiles_per_b;  // T > 1: row tiles per sequence; T == 1: 0
+  int m_tiles, n_tiles;
 };
 
 struct OpBars {
   uint64_t full[8];
   uint64_t empty[8];
-  uint64_t acc_full;
+  uint64_t acc_full[2];   // accumulator buffer a holds a finished tile
+  uint64_t acc_empty[2];  // accumulator buffer a read out (4 warp arrivals)
+  uint64_t mma_done;
   uint32_t tmem_base;
   int abort_flag;
 };
+
+// Output tile t: row tile t % m_tiles (rows (b, i0 .. i0 + 127) for T > 1, sequences
+// b .. b + 127 for T == 1), column tile t / m_tiles.  Row tiles run fastest, so the CTAs
+// resident at once share one weight column block in L2.
+struct OpTile {
+  int b, i0, n0;
+};
+__device__ __forceinline__ OpTile op_tile(const OprojParams& p, int t, int bn) {
+  OpTile w;
+  const int mt = t % p.m_tiles;
+  w.n0 = (t / p.m_tiles) * bn;
+  if (p.m_tiles_per_b > 0) {
+    w.b = mt / p.m_tiles_per_b;
+    w.i0 = (mt % p.m_tiles_per_b) * kOpBM;
+  } else {
+    w.b = mt * kOpBM;
+    w.i0 = 0;
+  }
+  return w;
+}
 
 template <int BN>
 __global__ void __launch_bounds__(256, 1) oproj_kernel(const __grid_constant__ OprojParams p) {
@@ -76,29 +102,24 @@ __global__ void __launch_bounds__(256, 1) oproj_kernel(const __grid_constant__ O
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int KB = p.K / kOpBK;
-
-  // This tile's rows: (b, i0 .. i0 + 127) for T > 1, sequences b0 .. b0 + 127 for T == 1.
-  const int mt = blockIdx.x;
-  const int n0 = blockIdx.y * BN;
-  int b = 0, i0 = 0;
-  if (p.m_tiles_per_b > 0) {
-    b = mt / p.m_tiles_per_b;
-    i0 = (mt % p.m_tiles_per_b) * kOpBM;
-  } else {
-    b = mt * kOpBM;
-  }
+  const int n_tiles = p.m_tiles * p.n_tiles;
+  const int G = gridDim.x;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bars->full[s], 1 + C::kWProd);  // the A producer and the weight producers
       mbar_init(&bars->empty[s], 1);
     }
-    mbar_init(&bars->acc_full, 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&bars->acc_full[a], 1);
+      mbar_init(&bars->acc_empty[a], 4);  // the 4 epilogue warps
+    }
+    mbar_init(&bars->mma_done, 1);
     bars->abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
-    tc::tmem_alloc(&bars->tmem_base, C::kTmemCols);
+    tc::tmem_alloc(&bars->tmem_base, 2 * C::kTmemCols);
     tc::tmem_relinquish();
   }
   tc::fence_before_sync();
@@ -109,104 +130,134 @@ __global__ void __launch_bounds__(256, 1) oproj_kernel(const __grid_constant__ O
   if ((warp == 0 || warp == 2 || warp == 3) && lane == 0) {
     // ================= TMA producers =================
     // warp 0: the A slice (16 KB); warps 2 and 3: weight rows n0 .. n0 + 127 and
-    // n0 + 128 .. n0 + 255 (BN = 256; warp 2 alone for narrower tiles).
+    // n0 + 128 .. n0 + 255 (BN = 256; warp 2 alone for narrower tiles).  The k-block ring
+    // runs on across the CTA's tiles.
     const int role = warp == 0 ? 0 : warp - 1;  // 0 = A, 1.. = weight box
     if (role <= C::kWProd) {
       prefetch_tmap(role == 0 ? (const void*)&p.tm_a : (const void*)&p.tm_w);
-      int posted = 0;
-      for (int kb = 0; kb < KB; ++kb) {
-        const int s = kb % C::kStages;
-        if (kb >= C::kStages &&
-            !mbar_wait(&bars->empty[s], ((kb / C::kStages) - 1) & 1, p.status, abort_flag))
-          break;
-        uint8_t* stage = smem + s * C::kStage;
-        if (role == 0) {
-          mbar_arrive_expect_tx(&bars->full[s], kOpASub);
-          const int h = kb >> 1, d0 = (kb & 1) * kOpBK;
-          if (p.m_tiles_per_b > 0)
-            tma_load_4d(stage, &p.tm_a, &bars->full[s], d0, i0, h, b);
-          else
-            tma_load_4d(stage, &p.tm_a, &bars->full[s], d0, 0, h, b);
-        } else {
-          mbar_arrive_expect_tx(&bars->full[s], C::kBoxN * kOpBK * 2);
-          const int r = (role - 1) * C::kBoxN;
-          tma_load_2d(stage + kOpASub + r * kOpBK * 2, &p.tm_w, &bars->full[s], kb * kOpBK,
-                      n0 + r);
+      uint32_t g = 0;  // k-blocks posted over the run
+      bool ok = true;
+      for (int t = blockIdx.x; t < n_tiles && ok; t += G) {
+        const OpTile w = op_tile(p, t, BN);
+        for (int kb = 0; kb < KB; ++kb, ++g) {
+          const int s = g % C::kStages;
+          if (g >= (uint32_t)C::kStages &&
+              !mbar_wait(&bars->empty[s], ((g / C::kStages) - 1) & 1, p.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* stage = smem + s * C::kStage;
+          if (role == 0) {
+            mbar_arrive_expect_tx(&bars->full[s], kOpASub);
+            const int h = kb >> 1, d0 = (kb & 1) * kOpBK;
+            tma_load_4d(stage, &p.tm_a, &bars->full[s], d0, w.i0, h, w.b);
+          } else {
+            mbar_arrive_expect_tx(&bars->full[s], C::kBoxN * kOpBK * 2);
+            const int r = (role - 1) * C::kBoxN;
+            tma_load_2d(stage + kOpASub + r * kOpBK * 2, &p.tm_w, &bars->full[s], kb * kOpBK,
+                        w.n0 + r);
+          }
         }
-        posted = kb + 1;
       }
       // Loads in flight must land before the CTA's shared memory is released.
-      for (int kb = max(0, posted - C::kStages); kb < posted; ++kb) {
-        const uint32_t a = smem_u32(&bars->full[kb % C::kStages]);
+      for (uint32_t k = g > (uint32_t)C::kStages ? g - C::kStages : 0; k < g; ++k) {
+        const uint32_t a = smem_u32(&bars->full[k % C::kStages]);
         const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(a, (kb / C::kStages) & 1))
+        while (!mbar_try_wait(a, (k / C::kStages) & 1))
           if (globaltimer_ns() - t0 > kWaitLimitNs) break;
       }
     }
   } else if (warp == 1) {
     // ================= MMA issuer =================
+    // Tile j of this CTA accumulates in TMEM buffer j & 1, once the epilogue has read the
+    // tile two back out of it.
     constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kOpBM, BN, false);
     const uint64_t dhi = tc::smem_desc_sw128(0, 16, 1024);
     const uint32_t base_lo = smem_u32(smem) >> 4;
     bool ok = true;
-    for (int kb = 0; kb < KB && ok; ++kb) {
-      const int s = kb % C::kStages;
-      ok = __all_sync(0xffffffffu,
-                      mbar_wait(&bars->full[s], (kb / C::kStages) & 1, p.status, abort_flag));
+    uint32_t g = 0;
+    int j = 0;
+    for (int t = blockIdx.x; t < n_tiles && ok; t += G, ++j) {
+      const int ab = j & 1;
+      if (j >= 2)
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->acc_empty[ab], ((j >> 1) - 1) & 1,
+                                               p.status, abort_flag));
       if (!ok) break;
       tc::fence_after_sync();
-      const uint32_t a_lo = base_lo + (s * C::kStage >> 4);
-      const uint32_t b_lo = a_lo + (kOpASub >> 4);
-      if (tc::elect_one()) {
+      const uint32_t acc = tbase + ab * C::kTmemCols;
+      for (int kb = 0; kb < KB; ++kb, ++g) {
+        const int s = g % C::kStages;
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(&bars->full[s], (g / C::kStages) & 1, p.status, abort_flag));
+        if (!ok) break;
+        tc::fence_after_sync();
+        const uint32_t a_lo = base_lo + (s * C::kStage >> 4);
+        const uint32_t b_lo = a_lo + (kOpASub >> 4);
+        if (tc::elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < kOpBK / 16; ++kk) {
-          const uint32_t koff = kk * (32 >> 4);
-          tc::mma_ss(tbase, dhi | (uint64_t)(a_lo + koff), dhi | (uint64_t)(b_lo + koff), kIdesc,
-                     (kb | kk) != 0 ? 1u : 0u);
+          for (int kk = 0; kk < kOpBK / 16; ++kk) {
+            const uint32_t koff = kk * (32 >> 4);
+            tc::mma_ss(acc, dhi | (uint64_t)(a_lo + koff), dhi | (uint64_t)(b_lo + koff),
+                       kIdesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc::commit(&bars->empty[s]);
+          if (kb == KB - 1) tc::commit(&bars->acc_full[ab]);
         }
-        tc::commit(&bars->empty[s]);
+        __syncwarp();
       }
-      __syncwarp();
     }
-    if (tc::elect_one()) tc::commit(&bars->acc_full);  // also after a failed wait: no MMA
-    __syncwarp();                                      // may still run at the dealloc
+    // No MMA may still run when TMEM is released (also after a failed wait).
+    if (tc::elect_one()) tc::commit(&bars->mma_done);
+    __syncwarp();
+    const uint32_t a = smem_u32(&bars->mma_done);
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(a, 0))
+      if (globaltimer_ns() - t0 > kWaitLimitNs) break;
   } else if (warp >= 4) {
     // ================= epilogue =================
     const int q = warp & 3;
     const int r = q * 32 + lane;  // tile row = TMEM lane
-    const bool got =
-        __all_sync(0xffffffffu, mbar_wait(&bars->acc_full, 0, p.status, abort_flag));
-    if (got) {
+    int j = 0;
+    for (int t = blockIdx.x; t < n_tiles; t += G, ++j) {
+      const int ab = j & 1;
+      const bool got = __all_sync(
+          0xffffffffu, mbar_wait(&bars->acc_full[ab], (j >> 1) & 1, p.status, abort_flag));
+      if (!got) break;
       tc::fence_after_sync();
+      const OpTile w = op_tile(p, t, BN);
       bool row_ok;
       size_t row;
       if (p.m_tiles_per_b > 0) {
-        row_ok = i0 + r < p.T;
-        row = (size_t)b * p.T + i0 + r;
+        row_ok = w.i0 + r < p.T;
+        row = (size_t)w.b * p.T + w.i0 + r;
       } else {
-        row_ok = b + r < p.B;
-        row = (size_t)(b + r);
+        row_ok = w.b + r < p.B;
+        row = (size_t)(w.b + r);
       }
-      uint16_t* dst = p.y + row * p.N + n0;
-      const uint32_t t_row = tbase + ((uint32_t)(q * 32) << 16);
+      uint16_t* dst = p.y + row * p.N + w.n0;
+      const uint32_t t_row = tbase + ab * C::kTmemCols + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
       for (int c = 0; c < BN / 16; ++c) {
         uint32_t v[16];
         tc::tmem_ld16(t_row + c * 16, v);
         tc::tmem_wait_ld();
-        if (row_ok && n0 + c * 16 < p.N) {
+        if (row_ok && w.n0 + c * 16 < p.N) {
           uint4* o = reinterpret_cast<uint4*>(dst + c * 16);
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(v[8 * u + 0]), __uint_as_float(v[8 * u + 1]));
-            w.y = pack_bf16x2(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3]));
-            w.z = pack_bf16x2(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5]));
-            w.w = pack_bf16x2(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7]));
-            o[u] = w;
+            uint4 x;
+            x.x = pack_bf16x2(__uint_as_float(v[8 * u + 0]), __uint_as_float(v[8 * u + 1]));
+            x.y = pack_bf16x2(__uint_as_float(v[8 * u + 2]), __uint_as_float(v[8 * u + 3]));
+            x.z = pack_bf16x2(__uint_as_float(v[8 * u + 4]), __uint_as_float(v[8 * u + 5]));
+            x.w = pack_bf16x2(__uint_as_float(v[8 * u + 6]), __uint_as_float(v[8 * u + 7]));
+            o[u] = x;
           }
         }
       }
+      // This warp's rows of the accumulator are read: the MMA warp may reuse the buffer.
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->acc_empty[ab]);
     }
   }
 
@@ -214,7 +265,7 @@ __global__ void __launch_bounds__(256, 1) oproj_kernel(const __grid_constant__ O
   __syncthreads();
   if (warp == 1) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tbase, C::kTmemCols);
+    tc::tmem_dealloc(tbase, 2 * C::kTmemCols);
   }
 }
 
@@ -278,6 +329,8 @@ cudaError_t launch_bn(const OprojArgs& a, int m_tiles, cudaStream_t stream) {
   p.N = a.N;
   p.K = a.H * 128;
   p.m_tiles_per_b = a.T > 1 ? (a.T + kOpBM - 1) / kOpBM : 0;
+  p.m_tiles = m_tiles;
+  p.n_tiles = (a.N + BN - 1) / BN;
   static std::atomic<uint64_t> attr_done{0};  // bit per device: smem attribute set
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -289,8 +342,11 @@ cudaError_t launch_bn(const OprojArgs& a, int m_tiles, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     attr_done.fetch_or(bit);
   }
-  const dim3 grid((unsigned)m_tiles, (unsigned)((a.N + BN - 1) / BN));
-  oproj_kernel<BN><<<grid, 256, C::kSmem, stream>>>(p);
+  // Persistent: one CTA per SM (at most one per tile), each walking tiles c, c + G, ...
+  const int sms = device_sm_count() > 0 ? device_sm_count() : 152;
+  const int64_t tiles = (int64_t)m_tiles * p.n_tiles;
+  if (tiles > 0x7fffffff) return cudaErrorInvalidValue;
+  oproj_kernel<BN><<<(unsigned)std::min<int64_t>(tiles, sms), 256, C::kSmem, stream>>>(p);
   return cudaGetLastError();
 }
 
