@@ -94,10 +94,20 @@ def peak_for(kind: str, sustained: bool):
     return FALLBACK_BF16_TFLOPS, "fallback 1.9 PFLOP/s bf16"
 
 
-def kernel_source_sha():
+# The sources a kernel's DRAM traffic depends on: its own file, the shared device headers,
+# and the host file where its launch plan is made.
+KERNEL_SOURCES = {
+    "mla_prefill_kernel": ("prefill.cu", "ptx.cuh", "tcgen05.cuh", "kernels.h"),
+    "decode_splitkv_kernel": ("decode.cu", "host.cu", "ptx.cuh", "kernels.h"),
+    "latent_splitkv_kernel": ("latent.cu", "host.cu", "ptx.cuh", "tcgen05.cuh", "kernels.h"),
+    "oproj_kernel": ("oproj.cu", "ptx.cuh", "tcgen05.cuh", "kernels.h"),
+}
+
+
+def kernel_source_sha(kernel: str):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_causal_attention_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    for fn in sorted(KERNEL_SOURCES[kernel]):
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode())
             h.update(f.read())
@@ -106,13 +116,13 @@ def kernel_source_sha():
 
 def recorded_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on this
-    workload with this source."""
+    workload with the kernel's current sources."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         e = d[kernel]
-        if e.get("source_sha256") != kernel_source_sha() or e.get("workload") != workload:
+        if e.get("source_sha256") != kernel_source_sha(kernel) or e.get("workload") != workload:
             return None
         return int(e["dram_bytes_per_launch"])
     except Exception:

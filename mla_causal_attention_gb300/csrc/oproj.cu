@@ -40,7 +40,7 @@ template <int BN>
 struct OpCfg {
   static constexpr int kBBytes = BN * kOpBK * 2;               // weight slice
   static constexpr int kStage = kOpASub + kBBytes;
-  static constexpr int kStages = BN == 256 ? 4 : 8;
+  static constexpr int kStages = BN == 256 ? 4 : (BN == 48 ? 10 : 8);  // fill shared memory
   static constexpr int kTmemCols = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
   static_assert(2 * kTmemCols <= 512, "two accumulators in TMEM");
   static_assert(kStage % 1024 == 0 && BN % 16 == 0, "stage alignment, MMA N");
@@ -61,9 +61,9 @@ struct OprojParams {
   int m_tiles, n_tiles;
 };
 
-struct OpBars {
-  uint64_t full[8];
-  uint64_t empty[8];
+struct OpBars {  // <= 256 bytes
+  uint64_t full[10];
+  uint64_t empty[10];
   uint64_t acc_full[2];   // accumulator buffer a holds a finished tile
   uint64_t acc_empty[2];  // accumulator buffer a read out (4 warp arrivals)
   uint64_t mma_done;
@@ -90,6 +90,8 @@ __device__ __forceinline__ OpTile op_tile(const OprojParams& p, int t, int bn) {
   }
   return w;
 }
+
+static_assert(sizeof(OpBars) <= 256, "barrier block");
 
 template <int BN>
 __global__ void __launch_bounds__(256, 1) oproj_kernel(const __grid_constant__ OprojParams p) {
