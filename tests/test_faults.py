@@ -41,3 +41,26 @@ def test_host_errors_raise():
     with pytest.raises(binding.MlaAttnError):
         mla_attn_fwd(d["q_nope"], d["q_pe"], d["k_nope"], d["k_pe_shared"], d["v"],
                      d["kv_len"], 0, -1.0)
+
+
+@pytest.mark.parametrize("bad", [0, 301, -5])
+def test_latent_out_of_range_kv_len_sets_status(bad):
+    """The latent path clamps kv_len into [1, Tk] for its partition and reports the bad value."""
+    from mla_causal_attention_gb300.inputs import make_latent_inputs
+    w = Workload("t", 3, 64, 1, 299, 1.0, (1, 300), softmax_scale_192())
+    inp = make_latent_inputs(w, seed=3)
+    d = {k: v.cuda() for k, v in inp.items()}
+    ws = binding.Workspace("cuda")
+    d["kv_len"][1] = bad
+
+    def call():
+        return binding.mla_latent_decode_fwd(d["q_nope"], d["q_pe"], d["c_kv"], d["k_pe"],
+                                             d["w_kvb"], d["kv_len"], w.softmax_scale,
+                                             workspace=ws)
+    out = call()
+    assert binding.mla_attn_get_status(ws) == binding.MlaStatus.ERR_KVLEN
+    assert binding.mla_attn_get_status(ws) == 0  # reading clears it
+    assert torch.isfinite(out.float()).all()
+    d["kv_len"][1] = 300
+    call()
+    assert binding.mla_attn_get_status(ws) == 0
