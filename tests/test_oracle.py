@@ -224,6 +224,17 @@ def test_workloads_match_printed_shapes():
     assert g["attention_dropout"] == 0.0  # dropout is the identity in this path
     inp = make_inputs(WORKLOADS["tiny_prefill"], seed=0)
     assert tuple(inp["v"].shape[1:]) == (64, 16, 128)
+    # the latent width and the output projection's width, without bias
+    from mla_causal_attention_gb300.workloads import D_LAT
+    assert D_LAT == g["kv_lora_rank"]
+    assert g["attention_bias"] is False
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "bench", os.path.join(os.path.dirname(GOLDEN), os.pardir, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    for c in bench.OPROJ_WORKLOADS.values():
+        assert c["N"] == g["hidden_size"] and c["H"] == g["num_attention_heads"]
 
 
 def test_oracle_rejects_bad_arguments():
