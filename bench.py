@@ -95,7 +95,7 @@ def peak_for(kind: str, sustained: bool):
 
 
 # The sources a kernel's DRAM traffic depends on: its own file, the shared device headers,
-# and the host file where its launch plan is made.
+# and the host file where its launch plan is made (their code, not their comments).
 KERNEL_SOURCES = {
     "mla_prefill_kernel": ("prefill.cu", "ptx.cuh", "tcgen05.cuh", "kernels.h"),
     "decode_splitkv_kernel": ("decode.cu", "host.cu", "ptx.cuh", "kernels.h"),
@@ -104,13 +104,21 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(src: str) -> str:
+    """The source without comments and with whitespace collapsed: what the compiler sees."""
+    import re
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
 def kernel_source_sha(kernel: str):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_causal_attention_gb300", "csrc")
     for fn in sorted(KERNEL_SOURCES[kernel]):
-        with open(os.path.join(csrc, fn), "rb") as f:
+        with open(os.path.join(csrc, fn), encoding="utf-8") as f:
             h.update(fn.encode())
-            h.update(f.read())
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()
 
 

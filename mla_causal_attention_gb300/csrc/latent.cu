@@ -33,12 +33,11 @@
 //   L[128, 64 heads]         += 1[128, 128] . P              the row sums, A = ones in TMEM
 // so O^T takes 4 x 64 TMEM columns (a head-major O would need all 512), and the softmax
 // needs no sum reduction: every row of L holds the running sum of each head's (bf16)
-// weights, rescaled with O^T.  The tile's eight
-// 64-column latent sub-tiles stay in eight fixed slots from the score pass through the
-// value pass (latent sub-tile s of every tile lives in slot s); its rotary-key sub-tile is
-// loaded into the P^T buffer, which is free during the score pass.  Each value block
-// releases its two slots, so the next tile's first sub-tiles load while the current value
-// mixes still run.
+// weights, rescaled with O^T.  The tile's eight 64-column latent sub-tiles stay in eight
+// fixed slots from the score pass through the value pass (latent sub-tile s of every tile
+// lives in slot s); its rotary-key sub-tile is loaded into the P buffer, which is free
+// during the score pass.  Each value block releases its two slots, so the next tile's first
+// sub-tiles load while the current value mixes still run.
 #include <cuda.h>
 
 #include <algorithm>
@@ -86,7 +85,7 @@ struct LatentParams {
 struct LBars {
   uint64_t full[kLSlots];   // slot s holds the current tile's latent sub-tile s
   uint64_t empty[kLSlots];  // slot s released by the value block that read it
-  uint64_t pe_full;         // the tile's rotary keys are in the P^T buffer
+  uint64_t pe_full;         // the tile's rotary keys are in the P buffer
   uint64_t pe_free;         // the previous tile's value mixes are done with P
   uint64_t q_full;
   uint64_t q_empty;         // the segment's last score MMA has read Q
