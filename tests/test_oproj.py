@@ -45,6 +45,8 @@ def _check(B, H, T, N, seed, rows=None, label=""):
     (3, 64, 16, 288),     # the tiny-prefill shape's 16 rows
     (5, 8, 1, 64),        # decode rows: 5 sequences
     (200, 4, 1, 320),     # decode rows over two 128-sequence tiles
+    (1, 1, 1, 32),        # the smallest: one head (two k-blocks), 32 outputs
+    (3, 1, 200, 32),      # one head, ragged row tiles, N below every column tile
 ])
 def test_oproj_matches_oracle(B, H, T, N):
     _check(B, H, T, N, seed=B * 7 + T)
