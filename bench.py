@@ -50,6 +50,8 @@ def parse_args():
                     help="decode over the latent cache, reported under secondary (or none)")
     ap.add_argument("--oproj", default="oproj_long_prefill",
                     help="output projection workload, reported under secondary (or none)")
+    ap.add_argument("--extended", action="store_true",
+                    help="also time the 2D-mask, append and rotary entry points (one GPU)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
@@ -505,6 +507,126 @@ def measure_oproj(name, args, rank, world, local, with_cpu):
     return res
 
 
+def _time_steps(call, args, local, stream, flush):
+    """Warm-up, then args.steps timed calls (L2 flushed before each, outside its events)."""
+    import torch
+
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            starts[i].record(stream)
+            call()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    return sum(step_ms) / len(step_ms), clk.summary()
+
+
+def measure_extended(args, local):
+    """The widening entry points on the bench's workloads (one GPU): the 2D key mask, the
+    fused KV-cache append and the rotary step with append.  Rates count algorithmic work
+    only (visible (query, key) pairs; bytes of visible keys)."""
+    import numpy as np
+    import torch
+
+    from mla_causal_attention_gb300 import binding
+    from mla_causal_attention_gb300.inputs import make_inputs
+    from mla_causal_attention_gb300.workloads import WORKLOADS, algorithmic_bytes
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device=dev)
+    keys = ("q_nope", "q_pe", "k_nope", "k_pe_shared", "v", "kv_len")
+    res = []
+
+    def line(name, value, unit, ms, bound, work, clocks, config, **extra):
+        peak, src = peak_for(bound, False)
+        achieved = value
+        res.append({"workload": name, "value": value, "unit": unit, "ms_per_step": ms,
+                    "roofline": {"bound": bound, "achieved": achieved, "peak": peak,
+                                 "unit": unit, "frac": achieved / peak, "traffic": None,
+                                 "peak_source": src, "algorithmic_per_launch": work},
+                    "clocks": clocks, "config": config, **extra})
+
+    # --- long prefill: 2D mask hiding the first 512 keys (left padding), rotary + append ---
+    wl = WORKLOADS["long_prefill"]
+    host = make_inputs(wl, seed=args.seed)
+    d = {k: host[k].to(dev) for k in keys}
+    out = torch.empty((wl.B, wl.H, wl.Tq, 128), dtype=torch.bfloat16, device=dev)
+    ws = binding.Workspace(dev)
+    pad = 512
+    mask = torch.ones((wl.B, wl.Tk), dtype=torch.uint8, device=dev)
+    mask[:, :pad] = 0
+    i = np.arange(wl.Tq, dtype=np.int64)
+    vis = np.maximum(0, np.minimum(i + wl.past_len + 1, wl.Tk) - pad).sum()
+    flops = 640.0 * wl.B * wl.H * vis
+    ms, clk = _time_steps(lambda: binding.mla_attn_masked_fwd(
+        d["q_nope"], d["q_pe"], d["k_nope"], d["k_pe_shared"], d["v"], None, mask, wl.past_len,
+        wl.softmax_scale, out=out, workspace=ws), args, local, stream, flush)
+    line("masked_long_prefill", flops / (ms * 1e-3) * 1e-12, "TFLOP/s", ms, "tensor", flops, clk,
+         {"workload": "long_prefill with the first 512 keys hidden by the 2D mask",
+          "visible_pairs": int(vis) * wl.B * wl.H})
+    table = binding.mla_rope_table(wl.Tk, device=dev)
+    caches = {k: torch.empty_like(d[k]) for k in ("k_nope", "v", "k_pe_shared")}
+    flops = 640.0 * wl.B * wl.H * (wl.Tq * (wl.Tq + 1) // 2)
+    ms, clk = _time_steps(lambda: binding.mla_attn_rope_append_fwd(
+        d["q_nope"], d["q_pe"], d["k_nope"], d["k_pe_shared"], d["v"], caches["k_nope"],
+        caches["k_pe_shared"], caches["v"], None, 0, wl.softmax_scale, table, out=out,
+        workspace=ws), args, local, stream, flush)
+    line("rope_append_long_prefill", flops / (ms * 1e-3) * 1e-12, "TFLOP/s", ms, "tensor", flops,
+         clk, {"workload": "long_prefill through the rotary step and the cache append "
+                           "(4096 new rows rotated and written, then attended)"})
+    del d, host, caches, out, ws
+
+    # --- ragged decode: random 10% holes in the 2D mask; fused append; rotary + append ---
+    wl = WORKLOADS["decode_ragged"]
+    host = make_inputs(wl, seed=args.seed)
+    d = {k: host[k].to(dev) for k in keys}
+    kv = host["kv_len"].numpy().astype(np.int64)
+    out = torch.empty((wl.B, wl.H, 1, 128), dtype=torch.bfloat16, device=dev)
+    ws = binding.Workspace(dev)
+    g = torch.Generator().manual_seed(args.seed)
+    mask_h = (torch.rand((wl.B, wl.Tk), generator=g) >= 0.1).to(torch.uint8)
+    mask_h[:, 0] = 1
+    mask = mask_h.to(dev)
+    live = mask_h.numpy().astype(bool) & (np.arange(wl.Tk)[None, :] < kv[:, None])
+    work_vis = algorithmic_bytes(wl, live.sum(axis=1))
+    work_all = algorithmic_bytes(wl, kv)
+    ms, clk = _time_steps(lambda: binding.mla_attn_masked_fwd(
+        d["q_nope"], d["q_pe"], d["k_nope"], d["k_pe_shared"], d["v"], d["kv_len"], mask,
+        wl.past_len, wl.softmax_scale, out=out, workspace=ws), args, local, stream, flush)
+    line("masked_decode_ragged", work_vis / (ms * 1e-3) * 1e-9, "GB/s", ms, "hbm", work_vis, clk,
+         {"workload": "decode_ragged with 10% of the keys hidden at random by the 2D mask"},
+         streamed_GBps=work_all / (ms * 1e-3) * 1e-9)
+    new = {"k_nope": d["k_nope"][:, :, -1:].clone(), "v": d["v"][:, :, -1:].clone(),
+           "k_pe_shared": d["k_pe_shared"][:, -1:].clone()}
+    ms, clk = _time_steps(lambda: binding.mla_attn_append_fwd(
+        d["q_nope"], d["q_pe"], new["k_nope"], new["k_pe_shared"], new["v"], d["k_nope"],
+        d["k_pe_shared"], d["v"], d["kv_len"], wl.past_len, wl.softmax_scale, out=out,
+        workspace=ws), args, local, stream, flush)
+    line("append_decode_ragged", work_all / (ms * 1e-3) * 1e-9, "GB/s", ms, "hbm", work_all, clk,
+         {"workload": "decode_ragged with the new token's rows appended to the cache in the "
+                      "same call"})
+    table = binding.mla_rope_table(wl.Tk, device=dev)
+    ms, clk = _time_steps(lambda: binding.mla_attn_rope_append_fwd(
+        d["q_nope"], d["q_pe"], new["k_nope"], new["k_pe_shared"], new["v"], d["k_nope"],
+        d["k_pe_shared"], d["v"], d["kv_len"], wl.past_len, wl.softmax_scale, table, out=out,
+        workspace=ws), args, local, stream, flush)
+    line("rope_append_decode_ragged", work_all / (ms * 1e-3) * 1e-9, "GB/s", ms, "hbm", work_all,
+         clk, {"workload": "decode_ragged with the rotary step on q_pe and the new k_pe, and "
+                           "the append, in the same call"})
+    if binding.mla_attn_get_status(ws, dev) != 0:
+        raise RuntimeError("device status set during the extended measurements")
+    del flush
+    return res
+
+
 def measure_e2e(wl, host, d, out, ws, stream, m, args, world):
     """Same metric through the public API from pinned host memory, copies included."""
     import torch
@@ -688,6 +810,7 @@ def main():
     opj = None
     if args.oproj and args.oproj != "none":
         opj = measure_oproj(args.oproj, args, rank, world, local, with_cpu=not args.no_cpu)
+    ext = measure_extended(args, local) if args.extended and world == 1 else []
     if rank == 0:
         m = workload_metrics(wl, [wl.Tk] * wl.B)
         line = base_line(args, wl, m, res["value"], res["ms_per_step"])
@@ -704,6 +827,8 @@ def main():
             line.setdefault("secondary", []).append(lat)
         if opj is not None:
             line.setdefault("secondary", []).append(opj)
+        for e in ext:
+            line.setdefault("secondary", []).append(e)
         print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -132,6 +132,7 @@ struct FixupArgs {
   const uint16_t* v;        // [B][H][kv_rows][128]
   uint16_t* out;            // [B][H][Tq][128]
   int B, H, Tq, Tk, past_len, kv_rows;
+  int heads_per_cta;        // set by the launcher
 };
 cudaError_t launch_masked_rows_fixup(const FixupArgs& a, cudaStream_t stream);
 

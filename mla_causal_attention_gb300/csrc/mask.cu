@@ -7,6 +7,7 @@
 // then has every score equal to that minimum, and its softmax weights are uniform over
 // all Tk keys: its output is the plain mean of the Tk value rows.  The attention kernels
 // skip hidden keys; masked_rows_fixup_kernel writes those uniform rows afterwards.
+#include <algorithm>
 #include <climits>
 #include <cstdint>
 
@@ -36,14 +37,18 @@ __global__ void __launch_bounds__(256) key_bits_kernel(const KeyBitsArgs a) {
   }
 }
 
-// One CTA of 256 threads per (sequence b, group of 8 heads).  Query row i of sequence b
-// sees no visible key when i + past_len is below the first key that is visible (key_mask
-// set and j < kv_len[b]).  Those rows get the mean of all Tk value rows.
+// One CTA of 256 threads per (16-column group cg, group of heads, sequence b).  Query row
+// i of sequence b sees no visible key when i + past_len is below the first key that is
+// visible (key_mask set and j < kv_len[b]).  Those rows get the mean of all Tk value rows.
+// Columns are split eight ways so that the whole read of V (every row of every head that
+// needs the mean) is spread over many SMs: each thread sums 8 columns of every 128th row.
 __global__ void __launch_bounds__(256) masked_rows_fixup_kernel(const FixupArgs a) {
   __shared__ int s_first;
-  __shared__ float s_part[8][128];
-  const int b = blockIdx.y;
-  const int h0 = blockIdx.x * 8;
+  __shared__ float s_part[8][16];
+  __shared__ float s_mean[16];
+  const int cg = blockIdx.x;  // columns [16 cg, 16 cg + 16)
+  const int h0 = blockIdx.y * a.heads_per_cta;
+  const int b = blockIdx.z;
   if (threadIdx.x == 0) s_first = INT_MAX;
   __syncthreads();
   int kvl = a.kv_len ? a.kv_len[b] : a.Tk;
@@ -62,37 +67,55 @@ __global__ void __launch_bounds__(256) masked_rows_fixup_kernel(const FixupArgs 
   if (n_rows == 0) return;  // uniform across the CTA
 
   const int lane = threadIdx.x & 31;
-  const int grp = threadIdx.x >> 5;  // 8 row groups
+  const int warp = threadIdx.x >> 5;
+  const int ch = threadIdx.x & 1;   // columns 16 cg + 8 ch .. + 8
+  const int r0 = threadIdx.x >> 1;  // rows r0, r0 + 128, ...
+  const int col = cg * 16 + ch * 8;
   const float inv_tk = 1.0f / (float)a.Tk;
-  for (int h = h0; h < min(h0 + 8, a.H); ++h) {
+  const int h1 = min(h0 + a.heads_per_cta, a.H);
+  for (int h = h0; h < h1; ++h) {
     const size_t bh = (size_t)b * a.H + h;
-    const uint16_t* vb = a.v + bh * a.kv_rows * 128;
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;  // columns 4 lane .. 4 lane + 3
-    for (int j = grp; j < a.Tk; j += 8) {
-      const uint2 w = *reinterpret_cast<const uint2*>(vb + (size_t)j * 128 + lane * 4);
-      s0 += bf16lo_to_f32(w.x);
-      s1 += bf16hi_to_f32(w.x);
-      s2 += bf16lo_to_f32(w.y);
-      s3 += bf16hi_to_f32(w.y);
+    const uint16_t* vb = a.v + bh * a.kv_rows * 128 + col;
+    float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int j = r0; j < a.Tk; j += 128) {
+      const uint4 w = *reinterpret_cast<const uint4*>(vb + (size_t)j * 128);
+      s[0] += bf16lo_to_f32(w.x);
+      s[1] += bf16hi_to_f32(w.x);
+      s[2] += bf16lo_to_f32(w.y);
+      s[3] += bf16hi_to_f32(w.y);
+      s[4] += bf16lo_to_f32(w.z);
+      s[5] += bf16hi_to_f32(w.z);
+      s[6] += bf16lo_to_f32(w.w);
+      s[7] += bf16hi_to_f32(w.w);
     }
-    s_part[grp][lane * 4 + 0] = s0;
-    s_part[grp][lane * 4 + 1] = s1;
-    s_part[grp][lane * 4 + 2] = s2;
-    s_part[grp][lane * 4 + 3] = s3;
+    // Lanes of one column half differ in bits 1..4.
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+#pragma unroll
+      for (int x = 2; x < 32; x <<= 1) s[k] += __shfl_xor_sync(0xffffffffu, s[k], x);
+    }
+    if (lane < 2) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) s_part[warp][lane * 8 + k] = s[k];
+    }
     __syncthreads();
-    if (threadIdx.x < 128) {
+    if (threadIdx.x < 16) {
       float t = 0.f;
 #pragma unroll
       for (int g = 0; g < 8; ++g) t += s_part[g][threadIdx.x];
-      s_part[0][threadIdx.x] = t * inv_tk;
+      s_mean[threadIdx.x] = t * inv_tk;
     }
     __syncthreads();
-    // Rows i < n_rows, 64 threads per row (2 columns each).
-    const int c = (threadIdx.x & 63) * 2;
-    const uint32_t word = pack_bf16x2(s_part[0][c], s_part[0][c + 1]);
-    for (int i = threadIdx.x >> 6; i < n_rows; i += 4)
-      *reinterpret_cast<uint32_t*>(a.out + (bh * a.Tq + i) * 128 + c) = word;
-    __syncthreads();  // s_part is reused by the next head
+    // Rows i < n_rows, two threads per row (8 columns each).
+    uint4 word;
+    word.x = pack_bf16x2(s_mean[ch * 8 + 0], s_mean[ch * 8 + 1]);
+    word.y = pack_bf16x2(s_mean[ch * 8 + 2], s_mean[ch * 8 + 3]);
+    word.z = pack_bf16x2(s_mean[ch * 8 + 4], s_mean[ch * 8 + 5]);
+    word.w = pack_bf16x2(s_mean[ch * 8 + 6], s_mean[ch * 8 + 7]);
+    for (int i = r0; i < n_rows; i += 128)
+      *reinterpret_cast<uint4*>(a.out + (bh * a.Tq + i) * 128 + col) = word;
+    __syncthreads();  // s_part and s_mean are reused by the next head
   }
 }
 
@@ -110,8 +133,13 @@ cudaError_t launch_key_bits(const KeyBitsArgs& a, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_masked_rows_fixup(const FixupArgs& a, cudaStream_t stream) {
-  dim3 grid((a.H + 7) / 8, a.B);
+cudaError_t launch_masked_rows_fixup(const FixupArgs& in, cudaStream_t stream) {
+  // Heads per CTA: one, unless 8 * B * H CTAs would be more than eight per SM.
+  FixupArgs a = in;
+  const int sms = device_sm_count() > 0 ? device_sm_count() : 152;
+  const long long ctas = 8LL * a.B * a.H;
+  a.heads_per_cta = (int)std::min<long long>(a.H, std::max<long long>(1, ctas / (8LL * sms)));
+  dim3 grid(8, (a.H + a.heads_per_cta - 1) / a.heads_per_cta, a.B);
   masked_rows_fixup_kernel<<<grid, 256, 0, stream>>>(a);
   return cudaGetLastError();
 }

@@ -124,6 +124,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 // decreasing sizes as well as dynamic assignment would, with no shared counter.
 struct Unit {
   int bh, b, r0, kvl, nt0, nt1, n;
+  int js;  // key tiles skipped at the front (hidden by the 2D mask); tile j is key tile j + js
   __device__ __forceinline__ int nt(int t) const { return t ? nt1 : nt0; }
 };
 
@@ -164,7 +165,29 @@ __device__ __forceinline__ Unit unit_make(const PrefillParams& p, int unit, int 
   w.nt0 = nt[0];
   w.nt1 = nt[1];
   w.n = max(nt[0], nt[1]);
+  w.js = 0;
   return w;
+}
+
+// Under the 2D mask, a leading key tile whose 128 keys are all hidden adds exactly nothing
+// to any row of the unit, so every role starts the unit at the first key tile with a
+// visible key.  The skip stops at the first query tile's last key tile, so that each query
+// tile keeps at least one key tile; a row left with no visible key at all is rewritten by
+// the masked-rows pass.  Each role reads the same packed bits, so all agree on js.
+template <bool kMasked>
+__device__ __forceinline__ void unit_skip_hidden(const PrefillParams& p, Unit& w) {
+  if (!kMasked) return;
+  const uint4* kb = reinterpret_cast<const uint4*>(p.key_bits) + (size_t)w.b * p.n_kt;
+  int js = 0;
+  while (js < w.nt0 - 1) {
+    const uint4 k = kb[js];
+    if ((k.x | k.y | k.z | k.w) != 0u) break;
+    ++js;
+  }
+  w.js = js;
+  w.nt0 -= js;
+  if (w.nt1 > 0) w.nt1 -= js;  // nt1 >= nt0 whenever tile 1 has rows
+  w.n -= js;
 }
 
 // kMasked: the 2D padding mask on keys is applied (p.key_bits); a separate instantiation so
@@ -264,12 +287,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; ok; ++i) {
         const int unit = unit_index(p, i);
         if (unit < 0) break;
-        const Unit w = unit_make(p, unit, kv_next);
+        Unit w = unit_make(p, unit, kv_next);
+        unit_skip_hidden<kMasked>(p, w);
         kv_next = unit_kv(p, unit_index(p, i + 1));  // fetched a unit ahead
         ok = load_q(i, 0, w.r0, w.nt0, w.bh);
         q_units = i + 1;
         for (int j = 0; j < w.n && ok; ++j, ++g, u += kSubPerKv) {
-          const int jt = j * kBN;
+          const int jt = (j + w.js) * kBN;
           // K(j): no-rope columns 0-63, 64-127 and the shared rotary tile, one barrier.
           uint64_t* kb = &bars->kfull[g & 1];
           for (int s = 0; s < 3 && ok; ++s) {
@@ -334,7 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; ok; ++i) {
         const int unit = unit_index(p, i);
         if (unit < 0) break;
-        const Unit w = unit_make(p, unit, kv_next);
+        Unit w = unit_make(p, unit, kv_next);
+        unit_skip_hidden<kMasked>(p, w);
         kv_next = unit_kv(p, unit_index(p, i + 1));  // fetched a unit ahead
         for (int j = 0; j <= w.n && ok; ++j) {
           const uint32_t gk = g + (uint32_t)j;           // key tile j of this unit
@@ -454,7 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; ok; ++i) {
       const int unit = unit_index(p, i);
       if (unit < 0) break;
-      const Unit w = unit_make(p, unit, kv_next);
+      Unit w = unit_make(p, unit, kv_next);
+      unit_skip_hidden<kMasked>(p, w);
       kv_next = unit_kv(p, unit_index(p, i + 1));  // fetched a unit ahead
       const int ntt = w.nt(t);
       const int qi = w.r0 + t * kBM + tw;  // query row within the sequence
@@ -467,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint4 kbits = make_uint4(~0u, ~0u, ~0u, ~0u);
         if (kMasked)
           kbits = *reinterpret_cast<const uint4*>(p.key_bits +
-                                                  ((size_t)w.b * p.n_kt + j) * 4);
+                                                  ((size_t)w.b * p.n_kt + j + w.js) * 4);
         ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_full[t], st & 1, p.status, abort_flag));
         if (!ok) break;
         tc::fence_after_sync();
@@ -478,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) pin32(r[c]);
 
-        const int jt = j * kBN;
+        const int jt = (j + w.js) * kBN;
         if (jt + kBN > limit) {
 #pragma unroll
           for (int c = 0; c < 4; ++c)

@@ -94,3 +94,20 @@ def test_long_prefill_left_padded_sampled():
     qs = sorted({0, 1, 699, 700, 701, 1023, 2048, 4095, *rng.integers(0, w.Tq, 8).tolist()})
     rows = [h * w.Tq + i for h in (0, 7) for i in qs]
     assert_close(gpu_rows(out, rows), _oracle(inp, mask, rows), "long_prefill left pad 700")
+
+
+@pytest.mark.parametrize("B,H,Tq,past,pads", [
+    (2, 4, 384, 200, (300, 520)),  # prefill: whole leading key tiles hidden (skipped)
+    (1, 4, 640, 0, (385,)),        # prefill from an empty cache: three tiles and one key
+    (5, 64, 1, 99, (100, 0, 3, 0, 0)),  # decode, sequence 0 sees nothing; B*H above the SMs
+    (20, 16, 16, 40, (56,)),       # prefill, sequence 0 sees nothing; B*H above the SMs
+])
+def test_left_padding_whole_tiles(B, H, Tq, past, pads):
+    """Left padding that covers whole 128-key tiles, and rows with nothing visible in
+    batches large enough that one pass over the value rows serves several heads."""
+    inp = make_inputs(Workload("t", B, H, Tq, past, 1.0, None, softmax_scale_192()), seed=34)
+    mask = np.ones((B, past + Tq), dtype=np.uint8)
+    for b, n in enumerate(pads):
+        mask[b, :n] = 0
+    out = _run(inp, mask)
+    assert_close(gpu_rows(out), _oracle(inp, mask), f"left pads {pads} B{B} H{H} Tq{Tq}")
