@@ -50,8 +50,9 @@ def parse_args():
                     help="decode over the latent cache, reported under secondary (or none)")
     ap.add_argument("--oproj", default="oproj_long_prefill",
                     help="output projection workload, reported under secondary (or none)")
-    ap.add_argument("--extended", action="store_true",
-                    help="also time the 2D-mask, append and rotary entry points (one GPU)")
+    ap.add_argument("--no-extended", dest="extended", action="store_false",
+                    help="skip the 2D-mask, append and rotary entry points (timed on one GPU "
+                         "and reported under secondary by default)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
