@@ -41,6 +41,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <mutex>
 
@@ -887,11 +888,12 @@ cudaError_t launch_latent(const LatentArgs& a, cudaStream_t stream) {
   p.seq_tile0 = a.seq_tile0;
   p.scale_log2 = a.scale_log2;
 
-  static int attr_device = -1;
+  static std::atomic<uint64_t> attr_done{0};  // bit per device: smem attributes set
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (attr_device != dev) {
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(attr_done.load(std::memory_order_acquire) & bit)) {
     e = cudaFuncSetAttribute(latent_splitkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kLSmem);
     if (e != cudaSuccess) return e;
@@ -901,13 +903,13 @@ cudaError_t launch_latent(const LatentArgs& a, cudaStream_t stream) {
     e = cudaFuncSetAttribute(latent_absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kAbsorbSmem);
     if (e != cudaSuccess) return e;
-    attr_device = dev;
+    attr_done.fetch_or(bit, std::memory_order_release);
   }
   const unsigned bgroups = (unsigned)((a.B + kPB - 1) / kPB);
   latent_absorb_kernel<<<dim3(a.H, kLD / kAbN, bgroups), 256, kAbsorbSmem, stream>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  // The other three start as programmatic dependents of the kernel before them.
+  // The other two start as programmatic dependents of the kernel before them.
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;

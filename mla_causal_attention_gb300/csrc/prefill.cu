@@ -35,6 +35,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <mutex>
 
@@ -840,18 +841,19 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   const uint64_t units = BH * (uint64_t)p.n_qb;
   if (units > 0x7fffffffull) return cudaErrorInvalidValue;
 
-  static int attr_device = -1;
+  static std::atomic<uint64_t> attr_done{0};  // bit per device: smem attribute set
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (attr_device != dev) {
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(attr_done.load(std::memory_order_acquire) & bit)) {
     e = cudaFuncSetAttribute(mla_prefill_kernel<false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(mla_prefill_kernel<true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_device = dev;
+    attr_done.fetch_or(bit, std::memory_order_release);
   }
   // Persistent: one CTA per SM (at most one per unit), each walking its units.
   const int sms = device_sm_count();
