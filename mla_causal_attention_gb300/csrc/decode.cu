@@ -207,17 +207,26 @@ __global__ void __launch_bounds__(DecCfg<G, T, NST, WPH>::kThreads, MINB)
   float l_run = 0.f;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
 
+  // 2D padding mask: the mask bytes of this lane's keys, loaded one stage ahead so that
+  // their latency never adds to a stage that has already landed.
+  uint8_t mnext[C::kPasses];
+  auto load_mask = [&](int it_m) {
+#pragma unroll
+    for (int ps = 0; ps < C::kPasses; ++ps) {
+      const int jm = j0 + it_m * T + wh * C::kTokPerWarp + ps * 4 + tk;
+      mnext[ps] = (KM && it_m < n_tiles && jm < j1) ? p.key_mask[(size_t)b * p.Tk + jm] : 1;
+    }
+  };
+  if (KM) load_mask(0);
+
   for (int it = 0; it < n_tiles; ++it) {
     const int slot = it % NST;
     const int jt = j0 + it * T;
     const int nt = min(T, j1 - jt);
-    // 2D padding mask: this lane's keys' bytes, fetched before the stage wait.
     bool hidden[C::kPasses];
 #pragma unroll
-    for (int ps = 0; ps < C::kPasses; ++ps) {
-      const int t = wh * C::kTokPerWarp + ps * 4 + tk;
-      hidden[ps] = KM && t < nt && p.key_mask[(size_t)b * p.Tk + jt + t] == 0;
-    }
+    for (int ps = 0; ps < C::kPasses; ++ps) hidden[ps] = KM && mnext[ps] == 0;
+    if (KM) load_mask(it + 1);
     if (!mbar_wait(&full[slot], (it / NST) & 1, p.status, abort_flag)) break;
     if (head_ok) {
       const uint8_t* st = stages + slot * C::kStageBytes;
