@@ -508,6 +508,24 @@ def measure_oproj(name, args, rank, world, local, with_cpu):
     return res
 
 
+def left_padded_visible_pairs(Tq: int, past_len: int, Tk: int, pad: int) -> int:
+    """Visible (query, key) pairs of one (b, h) when the 2D mask hides keys [0, pad): query i
+    sees keys [pad, min(i + past_len + 1, Tk))."""
+    import numpy as np
+
+    i = np.arange(Tq, dtype=np.int64)
+    return int(np.maximum(0, np.minimum(i + past_len + 1, Tk) - pad).sum())
+
+
+def visible_keys_per_sequence(key_mask, kv_len):
+    """Keys each decode sequence attends to: key_mask[b, j] set and j < kv_len[b]."""
+    import numpy as np
+
+    m = np.asarray(key_mask).astype(bool)
+    kv = np.asarray(kv_len, dtype=np.int64)
+    return (m & (np.arange(m.shape[1])[None, :] < kv[:, None])).sum(axis=1)
+
+
 def _time_steps(call, args, local, stream, flush):
     """Warm-up, then args.steps timed calls (L2 flushed before each, outside its events)."""
     import torch
@@ -564,8 +582,7 @@ def measure_extended(args, local):
     pad = 512
     mask = torch.ones((wl.B, wl.Tk), dtype=torch.uint8, device=dev)
     mask[:, :pad] = 0
-    i = np.arange(wl.Tq, dtype=np.int64)
-    vis = np.maximum(0, np.minimum(i + wl.past_len + 1, wl.Tk) - pad).sum()
+    vis = left_padded_visible_pairs(wl.Tq, wl.past_len, wl.Tk, pad)
     flops = 640.0 * wl.B * wl.H * vis
     ms, clk = _time_steps(lambda: binding.mla_attn_masked_fwd(
         d["q_nope"], d["q_pe"], d["k_nope"], d["k_pe_shared"], d["v"], None, mask, wl.past_len,
@@ -596,8 +613,7 @@ def measure_extended(args, local):
     mask_h = (torch.rand((wl.B, wl.Tk), generator=g) >= 0.1).to(torch.uint8)
     mask_h[:, 0] = 1
     mask = mask_h.to(dev)
-    live = mask_h.numpy().astype(bool) & (np.arange(wl.Tk)[None, :] < kv[:, None])
-    work_vis = algorithmic_bytes(wl, live.sum(axis=1))
+    work_vis = algorithmic_bytes(wl, visible_keys_per_sequence(mask_h.numpy(), kv))
     work_all = algorithmic_bytes(wl, kv)
     ms, clk = _time_steps(lambda: binding.mla_attn_masked_fwd(
         d["q_nope"], d["q_pe"], d["k_nope"], d["k_pe_shared"], d["v"], d["kv_len"], mask,
