@@ -62,3 +62,17 @@ def test_latent_ragged_batch_sampled():
     got = _gpu(d)
     rows = [b * 64 + h for b in range(16) for h in (0, 31, 63)]
     assert_close(got[rows], _oracle(d, rows), "latent B16 Tk8192 sampled")
+
+
+def test_latent_decode_ragged_full_size_sampled():
+    """The bench's latent workload (64 sequences x 64 heads, kv_len ~ U[512, 8192], its
+    generator and launch plan): twelve rows against the oracle."""
+    from mla_causal_attention_gb300.inputs import make_latent_inputs
+    from mla_causal_attention_gb300.workloads import LATENT_WORKLOADS
+    w = LATENT_WORKLOADS["latent_decode_ragged"]
+    d = make_latent_inputs(w, seed=0)
+    got = _gpu(d)
+    kv = d["kv_len"].numpy()
+    bs = sorted({int(np.argmin(kv)), int(np.argmax(kv)), 0, w.B - 1})
+    rows = [b * w.H + h for b in bs for h in (0, 31, w.H - 1)]
+    assert_close(got[rows], _oracle(d, rows), "latent_decode_ragged full, sampled")
