@@ -827,7 +827,14 @@ def main():
     opj = None
     if args.oproj and args.oproj != "none":
         opj = measure_oproj(args.oproj, args, rank, world, local, with_cpu=not args.no_cpu)
-    ext = measure_extended(args, local) if args.extended and world == 1 else []
+    ext = []
+    if args.extended and world == 1:
+        # These lines widen the report; a failure among them is reported, not allowed to
+        # take the primary line with it.
+        try:
+            ext = measure_extended(args, local)
+        except Exception as e:  # noqa: BLE001
+            ext = [{"workload": "extended", "error": f"{type(e).__name__}: {e}"}]
     if rank == 0:
         m = workload_metrics(wl, [wl.Tk] * wl.B)
         line = base_line(args, wl, m, res["value"], res["ms_per_step"])
