@@ -28,6 +28,7 @@ def test_decode_p1000_full(chunk):
     (4, 3, 0, None, 0),           # a single key
     (2, 64, 2047, (1, 2048), 256),
     (5, 4, 33, (30, 34), 64),
+    (300, 8, 63, (1, 64), 0),     # 600 head groups: the large configuration, one split
 ])
 def test_decode_small_full(B, H, past, kv, chunk):
     inp = make_inputs(wl(B, H, past, kv), seed=1)

@@ -32,6 +32,7 @@ def test_tiny_prefill_full():
     (2, 2, 300, 77, (200, 377)),  # padding inside the causal range, unaligned past_len
     (1, 4, 512, 1000, None),   # many key tiles before the diagonal
     (3, 2, 130, 126, (5, 256)),
+    (40, 8, 16, 10, (1, 26)),  # 320 units: every CTA walks several; kv_len ragged in [1, 26]
 ])
 def test_prefill_shapes_full(B, H, Tq, past, kv):
     inp = make_inputs(wl(B, H, Tq, past, kv), seed=5)
