@@ -47,6 +47,9 @@ def _check(B, H, T, N, seed, rows=None, label=""):
     (200, 4, 1, 320),     # decode rows over two 128-sequence tiles
     (1, 1, 1, 32),        # the smallest: one head (two k-blocks), 32 outputs
     (3, 1, 200, 32),      # one head, ragged row tiles, N below every column tile
+    (64, 8, 1, 4096),     # 64 decode rows, every one checked; ragged last column tile
+    (33, 16, 1, 7168),    # an odd decode batch at the model width, every row
+    (65, 4, 1, 96),       # 65 decode rows
 ])
 def test_oproj_matches_oracle(B, H, T, N):
     _check(B, H, T, N, seed=B * 7 + T)
