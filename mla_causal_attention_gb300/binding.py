@@ -145,15 +145,23 @@ def decode_plan(B: int, H: int, Tk: int):
 
 
 class Workspace:
-    """A zero-initialised device workspace sized for given shapes (grows on demand)."""
+    """A zero-initialised device workspace sized for given shapes (grows on demand).
+
+    A workspace serves one stream at a time: calls that may overlap on the GPU (on
+    different streams) need workspaces of their own.  The default one, used when a call
+    gets none, is shared by every call on its device.
+    """
 
     def __init__(self, device=None):
         self.device = torch.device(device or "cuda")
         self.buf = None
 
-    def get(self, nbytes: int) -> torch.Tensor:
+    def get(self, nbytes: int, stream=None) -> torch.Tensor:
+        """The buffer, at least nbytes long.  A new buffer is allocated and zero-filled on
+        `stream` (the one the call launches on), so the fill precedes the call's kernels."""
         if self.buf is None or self.buf.numel() < nbytes:
-            self.buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+            with torch.cuda.stream(stream):
+                self.buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=self.device)
         return self.buf
 
 
@@ -207,8 +215,8 @@ class PreparedCall:
             splits = -(-Tk // decode_chunk)
             ws_bytes = max(ws_bytes, 256 + (-(-B * H * splits * 8 // 256)) * 256
                            + B * H * splits * 512)
-        ws = (workspace or _default_workspace(dev)).get(ws_bytes)
         s = stream if stream is not None else torch.cuda.current_stream(dev)
+        ws = (workspace or _default_workspace(dev)).get(ws_bytes, stream=s)
         self.out = out
         self.device = dev
         self._keep = (q_nope, q_pe, k_nope, k_pe_shared, v, kv_len, out, ws, s)
@@ -269,9 +277,9 @@ def mla_attn_append_fwd(q_nope, q_pe, k_nope_new, k_pe_new, v_new, k_nope_cache,
     if out is None:
         out = torch.empty((B, H, Tq, 128), dtype=bf, device=dev)
     _check(out, "out", bf, (B, H, Tq, 128), dev)
-    ws = (workspace or _default_workspace(dev)).get(
-        lib.mla_attn_workspace_bytes(B, H, Tq, past_len + Tq))
     s = stream if stream is not None else torch.cuda.current_stream(dev)
+    ws = (workspace or _default_workspace(dev)).get(
+        lib.mla_attn_workspace_bytes(B, H, Tq, past_len + Tq), stream=s)
     with torch.cuda.device(dev):
         rc = lib.mla_attn_append_fwd(_ptr(q_nope), _ptr(q_pe), _ptr(k_nope_new),
                                      _ptr(k_pe_new), _ptr(v_new), _ptr(k_nope_cache),
@@ -309,9 +317,9 @@ def mla_attn_masked_fwd(q_nope, q_pe, k_nope, k_pe_shared, v, kv_len, key_mask,
     if out is None:
         out = torch.empty((B, H, Tq, 128), dtype=bf, device=dev)
     _check(out, "out", bf, (B, H, Tq, 128), dev)
-    ws = (workspace or _default_workspace(dev)).get(
-        lib.mla_attn_masked_workspace_bytes(B, H, Tq, Tk))
     s = stream if stream is not None else torch.cuda.current_stream(dev)
+    ws = (workspace or _default_workspace(dev)).get(
+        lib.mla_attn_masked_workspace_bytes(B, H, Tq, Tk), stream=s)
     with torch.cuda.device(dev):
         rc = lib.mla_attn_masked_fwd(_ptr(q_nope), _ptr(q_pe), _ptr(k_nope), _ptr(k_pe_shared),
                                      _ptr(v), _ptr(kv_len), _ptr(key_mask), B, H, Tq, Tk,
@@ -344,8 +352,9 @@ def mla_latent_decode_fwd(q_nope, q_pe, c_kv, k_pe, w_kvb, kv_len, softmax_scale
     if out is None:
         out = torch.empty((B, H, 128), dtype=bf, device=dev)
     _check(out, "out", bf, (B, H, 128), dev)
-    ws = (workspace or _default_workspace(dev)).get(lib.mla_latent_workspace_bytes(B, H, Tk))
     s = stream if stream is not None else torch.cuda.current_stream(dev)
+    ws = (workspace or _default_workspace(dev)).get(lib.mla_latent_workspace_bytes(B, H, Tk),
+                                                    stream=s)
     with torch.cuda.device(dev):
         rc = lib.mla_latent_decode_fwd(_ptr(q_nope), _ptr(q_pe), _ptr(c_kv), _ptr(k_pe),
                                        _ptr(w_kvb), _ptr(kv_len), B, H, Tk,
@@ -371,8 +380,9 @@ def mla_oproj_fwd(attn, w_o, out=None, workspace: "Workspace | None" = None, str
     if out is None:
         out = torch.empty((B, T, N), dtype=bf, device=dev)
     _check(out, "out", bf, (B, T, N), dev)
-    ws = (workspace or _default_workspace(dev)).get(lib.mla_oproj_workspace_bytes())
     s = stream if stream is not None else torch.cuda.current_stream(dev)
+    ws = (workspace or _default_workspace(dev)).get(lib.mla_oproj_workspace_bytes(),
+                                                    stream=s)
     with torch.cuda.device(dev):
         rc = lib.mla_oproj_fwd(_ptr(attn), _ptr(w_o), B, H, T, N, _ptr(out), _ptr(ws),
                                ws.numel(), ctypes.c_void_p(s.cuda_stream))
@@ -434,9 +444,9 @@ def mla_attn_rope_append_fwd(q_nope, q_pe_raw, k_nope_new, k_pe_new_raw, v_new, 
     if out is None:
         out = torch.empty((B, H, Tq, 128), dtype=bf, device=dev)
     _check(out, "out", bf, (B, H, Tq, 128), dev)
-    ws = (workspace or _default_workspace(dev)).get(
-        lib.mla_attn_rope_workspace_bytes(B, H, Tq, past_len + Tq))
     s = stream if stream is not None else torch.cuda.current_stream(dev)
+    ws = (workspace or _default_workspace(dev)).get(
+        lib.mla_attn_rope_workspace_bytes(B, H, Tq, past_len + Tq), stream=s)
     with torch.cuda.device(dev):
         rc = lib.mla_attn_rope_append_fwd(
             _ptr(q_nope), _ptr(q_pe_raw), _ptr(k_nope_new), _ptr(k_pe_new_raw), _ptr(v_new),
@@ -451,8 +461,8 @@ def mla_attn_rope_append_fwd(q_nope, q_pe_raw, k_nope_new, k_pe_new_raw, v_new, 
 def mla_attn_get_status(workspace: Workspace | None = None, device=None, stream=None) -> int:
     """Synchronise and read/clear the device status word (0 = no device-side error)."""
     dev = torch.device(device or "cuda")
-    ws = (workspace or _default_workspace(dev)).get(256)
     s = stream if stream is not None else torch.cuda.current_stream(dev)
+    ws = (workspace or _default_workspace(dev)).get(256, stream=s)
     with torch.cuda.device(dev):
         return int(library().mla_attn_get_status(_ptr(ws), ctypes.c_void_p(s.cuda_stream)))
 
