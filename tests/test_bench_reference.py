@@ -26,3 +26,19 @@ def test_reference_arm_line():
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_reference_arm_prints_on_rank_zero_only():
+    """Under a multi-process launch only rank 0 runs the oracle and prints; rank 1 exits 0
+    without output."""
+    outs = {}
+    for rank in (0, 1):
+        env = dict(os.environ, RANK=str(rank), LOCAL_RANK=str(rank), WORLD_SIZE="2",
+                   MASTER_ADDR="127.0.0.1", MASTER_PORT="29533")
+        r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload",
+                            "tiny_prefill", "--steps", "1", "--warmup", "0", "--gpus", "2"],
+                           cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+        assert r.returncode == 0, r.stderr[-2000:]
+        outs[rank] = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(outs[0]) == 1 and json.loads(outs[0][0])["impl"] == "reference"
+    assert outs[1] == []
