@@ -339,14 +339,20 @@ MLA_API mla_status mla_attn_decode_plan(int B, int H, int Tk, int* chunk, int* s
  *
  * Arguments and result are those of mla_attn_fwd with Tq = 1 and the same split plan, so
  * the output matches mla_attn_fwd's.  device_status (device int, may be NULL) receives
- * device-detected errors (MLA_ERR_KVLEN) the way the workspace status word does; the
- * caller zeroes and reads it.  Returns MLA_ERR_WORKSPACE when the plan for these sizes
- * needs more than the 32 MiB array (B * H * splits partials of 520 bytes each).
+ * device-detected errors (MLA_ERR_KVLEN, MLA_ERR_TIMEOUT) the way the workspace status
+ * word does; the caller zeroes and reads it.  Pass it: with device_status NULL those
+ * errors go unreported, and after a bounded wait gives up (a split that never wrote its
+ * partial) the merge may read partials a previous call left in the array, so the output
+ * is undefined without any sign of it.  Returns MLA_ERR_WORKSPACE when the plan for these
+ * sizes needs more than the 32 MiB array (B * H * splits partials of 520 bytes each).
  *
  * The call allocates nothing.  Its first call on a device looks up the array's device
- * address (cudaGetSymbolAddress) with that device current; make that first call before
- * any stream capture.  All calls share the array: calls that overlap on the GPU (other
- * streams, other host threads) race on it and must be serialised by the caller.
+ * address (cudaGetSymbolAddress) with that device current and keeps it for the rest of
+ * the process; make that first call before any stream capture.  The kept address belongs
+ * to the device's context of that time: after cudaDeviceReset on that device it is stale,
+ * so do not call this function on a device that has been reset since its first call.  All
+ * calls share the array: calls that overlap on the GPU (other streams, other host
+ * threads) race on it and must be serialised by the caller.
  */
 MLA_API mla_status mla_attn_decode_noalloc(const uint16_t* q_nope, const uint16_t* q_pe,
                                            const uint16_t* k_nope, const uint16_t* k_pe_shared,

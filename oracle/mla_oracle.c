@@ -490,13 +490,19 @@ typedef struct {
   int64_t n_rows;
   double* out;
   int64_t next;
+  int err;
   pthread_mutex_t lock;
 } oproj_job_t;
 
 static void* oproj_worker(void* arg) {
   oproj_job_t* J = (oproj_job_t*)arg;
   double* x = (double*)malloc((size_t)J->K * sizeof(double));
-  if (!x) return NULL;
+  if (!x) { /* reported: a row another worker does not pick up stays unwritten */
+    pthread_mutex_lock(&J->lock);
+    J->err = 3;
+    pthread_mutex_unlock(&J->lock);
+    return NULL;
+  }
   for (;;) {
     pthread_mutex_lock(&J->lock);
     const int64_t r = J->next++;
@@ -546,5 +552,5 @@ int mla_oracle_oproj_rows(const uint16_t* attn, const uint16_t* w, int64_t B, in
   if (started == 0) oproj_worker(&J);
   for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
   pthread_mutex_destroy(&J.lock);
-  return 0;
+  return J.err;
 }

@@ -1,5 +1,4 @@
 """Decode path (Tq == 1, split-KV + combine) against the fp64 oracle."""
-import numpy as np
 import pytest
 import torch
 
@@ -43,15 +42,13 @@ def test_decode_ragged_small_batch():
     assert_close(gpu_rows(out), oracle_for(inp), "decode_ragged B6")
 
 
-def test_decode_ragged_full_size_sampled():
-    """64 x 64 heads, kv_len in [512, 8192]: every head of 6 sequences vs the oracle."""
+def test_decode_ragged_full_size_every_row():
+    """Configuration 3 at its full size (64 x 64 heads, kv_len in [512, 8192]): every output
+    row against the oracle."""
     w = WORKLOADS["decode_ragged"]
     inp = make_inputs(w, seed=0)
     out = run_gpu(to_device(inp))
-    kv = inp["kv_len"].numpy()
-    bs = sorted({int(np.argmin(kv)), int(np.argmax(kv)), 0, 17, 40, 63})
-    rows = [b * w.H + h for b in bs for h in range(w.H)]
-    assert_close(gpu_rows(out, rows), oracle_for(inp, rows), "decode_ragged full, sampled")
+    assert_close(gpu_rows(out), oracle_for(inp), "decode_ragged every row")
 
 
 def test_decode_single_key_is_exact():
