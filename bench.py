@@ -3,15 +3,18 @@
 
 One JSON line per run (rank 0).  The headline workload is the long causal prefill
 (B=1, H=64, Tq=Tk=4096, dims 192/128, k_pe shared, inputs N(0,1)*0.5) measured in
-TFLOP/s of visible (query, key) pairs; the batched ragged decode (B=64, H=64,
-kv_len ~ U[512, 8192]) is reported in the same line under "secondary" in GB/s of
-algorithmic HBM bytes.  Every step is one call of the library's C ABI on inputs already
-resident in device memory; L2 is flushed (a 2x-L2 write) before every timed step, outside
-the step's CUDA events.  "e2e" repeats the measurement through the public API from pinned
-host buffers, host->device copies and the device->host read of the output included.
+TFLOP/s of visible (query, key) pairs.  The other four attention workloads (ragged decode,
+tiny prefill, the page's decode at 1000 cached keys, chunked prefill), the latent-cache
+decode, the output projection and the widening entry points (2D mask, append, rotary step)
+ride in the same line under "secondary": one short object per workload, last in the line
+(value, unit, ms per call, fraction of the measured peak, bound, median SM clock, the CPU
+oracle's rate).  Every step is one call of the library's C ABI on inputs already resident
+in device memory; L2 is flushed (a 2x-L2 write) before every timed step, outside the
+step's CUDA events.  "e2e" repeats the headline measurement through the public API from
+pinned host buffers, host->device copies and the device->host read of the output included.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME] [--secondary NAME|none]
+                  [--workload NAME] [--secondary NAME,NAME|none]
 
 --impl reference times the fp64 CPU oracle (the correctness reference, run as it stands)
 on the host cores on a bounded sample of the same workload.  Under torchrun each rank
@@ -45,11 +48,15 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="long_prefill")
-    ap.add_argument("--secondary", default="decode_ragged")
+    ap.add_argument("--secondary", default="decode_ragged,tiny_prefill,decode_p1000,"
+                                           "chunked_prefill",
+                    help="comma-separated attention workloads reported under secondary "
+                         "(or none)")
     ap.add_argument("--latent", default="latent_decode_ragged",
                     help="decode over the latent cache, reported under secondary (or none)")
-    ap.add_argument("--oproj", default="oproj_long_prefill",
-                    help="output projection workload, reported under secondary (or none)")
+    ap.add_argument("--oproj", default="oproj_long_prefill,oproj_decode_b64",
+                    help="comma-separated output projection workloads, reported under "
+                         "secondary (or none)")
     ap.add_argument("--no-extended", dest="extended", action="store_false",
                     help="skip the 2D-mask, append and rotary entry points (timed on one GPU "
                          "and reported under secondary by default)")
@@ -236,7 +243,7 @@ def launches_per_call(wl):
     return 1 if splits == 1 else 2
 
 
-def measure_ours(wl, args, rank, world, local, with_cpu):
+def measure_ours(wl, args, rank, world, local, with_cpu, with_e2e=True, cpu_seconds=None):
     import numpy as np
     import torch
 
@@ -311,10 +318,10 @@ def measure_ours(wl, args, rank, world, local, with_cpu):
         "work_per_step": m["work"],
     }
 
-    if not args.no_e2e:
+    if with_e2e and not args.no_e2e:
         res["e2e"] = measure_e2e(wl, host, d, out, ws, stream, m, args, world)
     if with_cpu and rank == 0 and world == 1:
-        res["cpu_baseline"] = cpu_baseline(wl, host, m, args.cpu_seconds)
+        res["cpu_baseline"] = cpu_baseline(wl, host, m, cpu_seconds or args.cpu_seconds)
     del flush
     return res
 
@@ -793,6 +800,40 @@ def workload_config(wl, args):
             "parallelism": f"replicas x{args.gpus}" if args.gpus > 1 else "single GPU"}
 
 
+def _names(arg):
+    if not arg or arg == "none":
+        return []
+    return [n for n in arg.split(",") if n]
+
+
+def _r(x, digits=4):
+    """x to `digits` significant digits (short JSON)."""
+    if x is None or not isinstance(x, (int, float)) or x == 0 or not math.isfinite(x):
+        return x
+    return float(f"{x:.{digits}g}")
+
+
+def compact(res):
+    """One short secondary entry from a measurement result."""
+    rf = res.get("roofline") or {}
+    c = {"v": _r(res.get("value")), "u": res.get("unit"), "ms": _r(res.get("ms_per_step")),
+         "frac": _r(rf.get("frac"), 3), "bound": rf.get("bound"), "peak": rf.get("peak")}
+    if rf.get("traffic"):
+        c["traffic"] = rf["traffic"]
+    clk = res.get("clocks") or {}
+    if clk:
+        c["mhz"] = clk.get("sm_mhz")
+        if clk.get("reasons"):
+            c["thr"] = clk["reasons"]
+    cpu = res.get("cpu_baseline")
+    if cpu:
+        c["cpu"] = _r(cpu.get("value"), 3)
+    for k in ("streamed_GBps",):
+        if k in res:
+            c["streamed"] = _r(res[k])
+    return c
+
+
 def main():
     args = parse_args()
     rank, world, local = dist_env()
@@ -816,25 +857,33 @@ def main():
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local))
         build_library()
     res = measure_ours(wl, args, rank, world, local, with_cpu=not args.no_cpu)
-    sec = None
-    if args.secondary and args.secondary != "none" and args.secondary != args.workload:
-        swl = WORKLOADS[args.secondary]
-        sec = measure_ours(swl, args, rank, world, local, with_cpu=not args.no_cpu)
-        sec["config"] = workload_config(swl, args)
-    lat = None
-    if args.latent and args.latent != "none":
-        lat = measure_latent(args.latent, args, rank, world, local, with_cpu=not args.no_cpu)
-    opj = None
-    if args.oproj and args.oproj != "none":
-        opj = measure_oproj(args.oproj, args, rank, world, local, with_cpu=not args.no_cpu)
-    ext = []
-    if args.extended and world == 1:
-        # These lines widen the report; a failure among them is reported, not allowed to
-        # take the primary line with it.
+    sec = {}
+
+    def guarded(name, fn):
+        # A failure in a secondary line is reported in its place, not allowed to take the
+        # headline line with it.
         try:
-            ext = measure_extended(args, local)
+            sec[name] = compact(fn())
         except Exception as e:  # noqa: BLE001
-            ext = [{"workload": "extended", "error": f"{type(e).__name__}: {e}"}]
+            sec[name] = {"error": f"{type(e).__name__}: {e}"[:200]}
+
+    for name in _names(args.secondary):
+        if name != args.workload:
+            guarded(name, lambda n=name: measure_ours(
+                WORKLOADS[n], args, rank, world, local, with_cpu=not args.no_cpu,
+                with_e2e=False, cpu_seconds=min(args.cpu_seconds, 4.0)))
+    for name in _names(args.latent):
+        guarded(name, lambda n=name: measure_latent(n, args, rank, world, local,
+                                                    with_cpu=not args.no_cpu))
+    for name in _names(args.oproj):
+        guarded(name, lambda n=name: measure_oproj(n, args, rank, world, local,
+                                                   with_cpu=not args.no_cpu))
+    if args.extended and world == 1:
+        try:
+            for e in measure_extended(args, local):
+                sec[e["workload"]] = compact(e)
+        except Exception as e:  # noqa: BLE001
+            sec["extended"] = {"error": f"{type(e).__name__}: {e}"[:200]}
     if rank == 0:
         m = workload_metrics(wl, [wl.Tk] * wl.B)
         line = base_line(args, wl, m, res["value"], res["ms_per_step"])
@@ -844,16 +893,10 @@ def main():
                 line[k] = res[k]
         line["step_ms_min"] = res["step_ms_min"]
         line["step_ms_max"] = res["step_ms_max"]
-        if sec is not None:
-            line["secondary"] = [{"workload": args.secondary, **{k: v for k, v in sec.items()
-                                                                if k != "work_per_step"}}]
-        if lat is not None:
-            line.setdefault("secondary", []).append(lat)
-        if opj is not None:
-            line.setdefault("secondary", []).append(opj)
-        for e in ext:
-            line.setdefault("secondary", []).append(e)
-        print(json.dumps(line))
+        # Last in the line, one short object per workload: value, unit, ms per call,
+        # fraction of the measured peak, bound, median SM clock, the CPU oracle's rate.
+        line["secondary"] = sec
+        print(json.dumps(line, separators=(",", ":")))
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0

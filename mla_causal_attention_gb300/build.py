@@ -67,5 +67,31 @@ def build_library(force: bool = False, verbose: bool = False, extra_flags=()) ->
     return LIB
 
 
+def build_test_variant(name: str, source: str, defines) -> str:
+    """A test-only copy of the library in which `source` is compiled with extra -D
+    defines (the other objects are the library's own).  It lives under _build/test_<name>/
+    and is never what the package loads; the product build sets none of these defines."""
+    build_library()
+    out_dir = os.path.join(BUILD, f"test_{name}")
+    os.makedirs(out_dir, exist_ok=True)
+    lib = os.path.join(out_dir, f"libmla_attn_{name}.so")
+    if os.path.exists(lib) and os.path.getmtime(lib) >= os.path.getmtime(LIB):
+        return lib
+    cc = nvcc()
+    obj = os.path.join(out_dir, source.replace(".cu", ".o"))
+    r = subprocess.run([cc, *_flags(defines), "-c", os.path.join(CSRC, source), "-o", obj],
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed for {source} ({name}):\n{r.stderr}")
+    objs = [obj if s == source else os.path.join(BUILD, s.replace(".cu", ".o")) for s in SOURCES]
+    tmp = lib + f".tmp{os.getpid()}"
+    r = subprocess.run([cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs,
+                        "-Xlinker", "--exclude-libs,ALL"], capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed ({name}):\n{r.stderr}")
+    os.replace(tmp, lib)
+    return lib
+
+
 if __name__ == "__main__":
     print(build_library(force="--force" in sys.argv, verbose="-v" in sys.argv))

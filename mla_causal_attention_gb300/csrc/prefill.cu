@@ -588,7 +588,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::tmem_wait_st();
         tc::fence_before_sync();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->p_ready[t]);
+#ifdef MLA_TEST_DROP_P_READY
+        // Test build only: the first softmax warp of CTA 0 withholds its P-ready arrival on
+        // the second key tile of its first unit.  The MMA warp's bounded wait for it then
+        // gives up, which exercises the timeout report and the CTA's unwinding (no copy or
+        // MMA left in flight, TMEM released).  The arrival carries no transaction bytes.
+        const bool withhold = blockIdx.x == 0 && i == 0 && j == 1 && warp == 4;
+#else
+        constexpr bool withhold = false;
+#endif
+        if (lane == 0 && !withhold) mbar_arrive(&bars->p_ready[t]);
       }
       if (!ok) break;
       // The unit's output: wait for the last value mix, move O_t to registers, release

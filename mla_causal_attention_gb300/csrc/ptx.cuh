@@ -10,7 +10,12 @@ namespace mla {
 
 // Upper bound on any single wait inside a kernel (nanoseconds of %globaltimer).  A wait
 // that runs past it records MLA_ERR_TIMEOUT in the status word and the kernel unwinds.
-constexpr uint64_t kWaitLimitNs = 1000000000ull;
+// MLA_WAIT_LIMIT_NS overrides it only in the test build that checks this unwinding; the
+// library itself is always built with the default.
+#ifndef MLA_WAIT_LIMIT_NS
+#define MLA_WAIT_LIMIT_NS 1000000000ull
+#endif
+constexpr uint64_t kWaitLimitNs = MLA_WAIT_LIMIT_NS;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
