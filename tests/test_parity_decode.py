@@ -51,6 +51,20 @@ def test_decode_ragged_full_size_every_row():
     assert_close(gpu_rows(out), oracle_for(inp), "decode_ragged every row")
 
 
+def test_decode_calls_with_changing_plans_share_a_workspace():
+    """Calls of different shapes and split plans follow one another on one workspace: each
+    call overwrites every partial it reads."""
+    from mla_causal_attention_gb300 import binding
+    ws = binding.Workspace()
+    cases = [wl(8, 64, 2047, (100, 2048)), wl(1, 64, 1000), wl(3, 5, 299, (1, 300)),
+             wl(8, 64, 2047, (100, 2048))]
+    for k, w in enumerate(cases):
+        inp = make_inputs(w, seed=40 + k)
+        out = run_gpu(to_device(inp), workspace=ws)
+        assert binding.mla_attn_get_status(ws) == 0
+        assert_close(gpu_rows(out), oracle_for(inp), f"decode sequence call {k}")
+
+
 def test_decode_single_key_is_exact():
     inp = make_inputs(wl(3, 8, 40, (1, 1)), seed=2)
     inp["kv_len"][:] = 1
