@@ -208,6 +208,10 @@ mla_status launch_fixup(const uint8_t* key_mask, const int32_t* kv_len, const ui
   return launch_masked_rows_fixup(f, stream) == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
+bool prefill_can_fuse_append(int past_len, const int32_t* kv_len, const uint8_t* key_mask) {
+  return past_len % 128 == 0 && kv_len == nullptr && key_mask == nullptr;
+}
+
 struct AppendPtrs {
   const uint16_t* new_k_nope;
   const uint16_t* new_k_pe;
@@ -242,7 +246,10 @@ mla_status attention_impl(const uint16_t* q_nope, const uint16_t* q_pe, const ui
   if (path < MLA_PATH_AUTO || path > MLA_PATH_DECODE) return MLA_ERR_ARG;
   if (path == MLA_PATH_AUTO) path = (Tq == 1) ? MLA_PATH_DECODE : MLA_PATH_PREFILL;
   if (path == MLA_PATH_DECODE && Tq != 1) return MLA_ERR_ARG;
-  if (app && path != MLA_PATH_DECODE) return MLA_ERR_ARG;
+  // The prefill kernel fuses the append only for a prefix of whole 128-key tiles and
+  // sequences without kv_len (every new row is then read by the unit that writes it).
+  if (app && path != MLA_PATH_DECODE && !prefill_can_fuse_append(past_len, kv_len, key_mask))
+    return MLA_ERR_ARG;
   int sms = 0;
   st = check_device(&sms);
   if (st != MLA_OK) return st;
@@ -301,6 +308,11 @@ mla_status attention_impl(const uint16_t* q_nope, const uint16_t* q_pe, const ui
   a.scale_log2 = scale_log2;
   a.kv_rows = kv_rows;
   a.key_bits = key_bits;
+  if (app) {
+    a.new_k_nope = app->new_k_nope;
+    a.new_k_pe = app->new_k_pe;
+    a.new_v = app->new_v;
+  }
   if (launch_prefill(a, stream) != cudaSuccess) return MLA_ERR_CUDA;
   return key_mask ? launch_fixup(key_mask, kv_len, v, out, B, H, Tq, Tk, past_len, kv_rows,
                                  stream)
@@ -344,8 +356,16 @@ mla_status mla_attn_append_fwd(const uint16_t* q_nope, const uint16_t* q_pe,
                           past_len, softmax_scale, out, workspace, workspace_bytes, cuda_stream,
                           nullptr, T_cap, &app);
   }
-  // Prefill: the checks run first (nothing is enqueued on failure), then the copy kernel
-  // appends the new rows, then attention reads the cache.
+  if (prefill_can_fuse_append(past_len, kv_len, nullptr)) {
+    // Prefill on a prefix of whole key tiles: the attention kernel reads the new rows where
+    // they are and writes them into the caches itself.
+    AppendPtrs app = {k_nope_new, k_pe_new, v_new, k_nope_cache, k_pe_cache, v_cache};
+    return attention_impl(q_nope, q_pe, k_nope_cache, k_pe_cache, v_cache, kv_len, B, H, Tq, Tk,
+                          past_len, softmax_scale, out, workspace, workspace_bytes, cuda_stream,
+                          nullptr, T_cap, &app);
+  }
+  // Other prefills: the checks run first (nothing is enqueued on failure), then the copy
+  // kernel appends the new rows, then attention reads the cache.
   mla_status st = attention_impl(q_nope, q_pe, k_nope_cache, k_pe_cache, v_cache, kv_len, B, H,
                                  Tq, Tk, past_len, softmax_scale, out, workspace,
                                  workspace_bytes, cuda_stream, nullptr, T_cap, nullptr, true);
@@ -418,9 +438,12 @@ mla_status mla_attn_rope_append_fwd(const uint16_t* q_nope, const uint16_t* q_pe
   uint16_t* q_pe_rot = reinterpret_cast<uint16_t*>(rot);
   uint16_t* k_pe_rot = reinterpret_cast<uint16_t*>(rot + q_rot_bytes(B, H, Tq));
 
-  // Every check of the attention call runs before anything is enqueued.
+  // Every check of the attention call runs before anything is enqueued.  Decode, and a
+  // prefill on a prefix of whole key tiles without kv_len, append inside the attention
+  // kernel (from the rotated keys in the workspace); other prefills copy first.
   AppendPtrs app = {k_nope_new, k_pe_rot, v_new, k_nope_cache, k_pe_cache, v_cache};
-  const AppendPtrs* fused = Tq == 1 ? &app : nullptr;
+  const bool fuse = Tq == 1 || prefill_can_fuse_append(past_len, kv_len, nullptr);
+  const AppendPtrs* fused = fuse ? &app : nullptr;
   mla_status st = attention_impl(q_nope, q_pe_rot, k_nope_cache, k_pe_cache, v_cache, kv_len, B,
                                  H, Tq, Tk, past_len, softmax_scale, out, workspace,
                                  workspace_bytes, cuda_stream, nullptr, T_cap, fused, true);
@@ -430,9 +453,9 @@ mla_status mla_attn_rope_append_fwd(const uint16_t* q_nope, const uint16_t* q_pe
   r.q_pe_raw = q_pe_raw; r.q_pe_rot = q_pe_rot; r.k_pe_raw = k_pe_new_raw;
   r.cos_sin = rope_table;
   r.B = B; r.H = H; r.Tq = Tq; r.past_len = past_len; r.kv_rows = T_cap;
-  if (Tq == 1) {
-    // Decode: rotate into the workspace; the decode kernel appends all three new rows.
-    r.k_pe_dst = k_pe_rot; r.k_pe_rows = 1; r.k_pe_row0 = 0;
+  if (fuse) {
+    // Rotate into the workspace; the attention kernel appends all three new rows.
+    r.k_pe_dst = k_pe_rot; r.k_pe_rows = Tq; r.k_pe_row0 = 0;
   } else {
     r.k_pe_dst = k_pe_cache; r.k_pe_rows = T_cap; r.k_pe_row0 = past_len;
     r.new_k_nope = k_nope_new; r.new_v = v_new;

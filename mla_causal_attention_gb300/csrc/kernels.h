@@ -74,6 +74,14 @@ struct PrefillArgs {
   // Optional 2D padding mask packed by launch_key_bits: [B][ceil(Tk/128)][4] words, bit e
   // of word c of key tile t = visibility of key 128 t + 32 c + e.  Null: no mask.
   const uint32_t* key_bits;
+  // Optional fused cache append (all null otherwise; needs past_len a multiple of 128 and
+  // no kv_len): key tiles from past_len / 128 on are read from the new rows
+  // ([B,H,Tq,128], [B,Tq,64], [B,H,Tq,128]) instead of k_nope / k_pe / v, and the unit that
+  // holds each such tile on its diagonal writes it into the caches (the same buffers as
+  // k_nope / k_pe / v, kv_rows rows per (b, h) or b) at rows [past_len, past_len + Tq).
+  const uint16_t* new_k_nope;
+  const uint16_t* new_k_pe;
+  const uint16_t* new_v;
 };
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream);

@@ -23,6 +23,11 @@
 //                 O_t += P_t V_j       8 x (M128 N128 K16), P from TMEM, V from smem.
 //               Order per key tile: PV_0(j-1), QK_0(j), PV_1(j-1), QK_1(j), so one
 //               softmax warpgroup works while the tensor core runs the other tile.
+//   warps 2, 3  only with the fused cache append: the unit that holds a new key tile on
+//               its diagonal writes it from shared memory into the caches (warp 2 the
+//               key sub-tiles, warp 3 the value sub-tiles, tensor stores issued as soon as
+//               the tile lands); the other units' tiles they just pass on.  The ring slots
+//               of a tile are released once both its MMAs and its stores have read them.
 //   warps 4-7   softmax of query tile 0 (thread = row = TMEM lane);
 //   warps 8-11  softmax of query tile 1.  Each reads its S row from TMEM, applies the
 //               causal/padding mask only on tiles that straddle the limit, keeps a
@@ -64,6 +69,15 @@ struct PrefillParams {
   CUtensorMap tm_kn;  // k_nope  {128, Tk, B*H}
   CUtensorMap tm_kr;  // k_pe    {64,  Tk, B}
   CUtensorMap tm_v;   // v       {128, Tk, B*H}
+  // Fused cache append only: the new rows (loads) and the caches' rows [0, Tk) (stores).
+  CUtensorMap tm_kn_new;  // new k_nope {128, Tq, B*H}
+  CUtensorMap tm_kr_new;  // new k_pe   {64,  Tq, B}
+  CUtensorMap tm_v_new;   // new v      {128, Tq, B*H}
+  CUtensorMap tm_kn_st;   // k_nope cache {128, Tk, B*H}
+  CUtensorMap tm_kr_st;   // k_pe cache   {64,  Tk, B}
+  CUtensorMap tm_v_st;    // v cache      {128, Tk, B*H}
+  int append;  // 1: key tiles n_pre.. come from the new rows and are written to the caches
+  int n_pre;   // key tiles of the cached prefix (past_len / 128)
   const int32_t* kv_len;
   const uint32_t* key_bits;  // packed 2D padding mask [B][n_kt][4], or null
   uint16_t* out;
@@ -117,6 +131,31 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   while (!mbar_try_wait(a, parity)) {
     if (globaltimer_ns() - t0 > kWaitLimitNs) return;
   }
+}
+
+// Tensor store shared -> global of one 128-byte swizzled box (no negative coordinates; the
+// map clips rows past its extent), and the bulk-group bookkeeping around it.
+__device__ __forceinline__ void tma_store_3d(const void* tmap, const void* smem_src, int c0,
+                                             int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+          tmap),
+      "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(smem_src))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// The source shared memory of every committed store has been read.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Every committed store has completed.
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // One work unit: a pair of 128-row query tiles of one (b, h).  Units are numbered
@@ -211,8 +250,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->kfull[i], 1);
       mbar_init(&bars->vfull[i], 1);
-      mbar_init(&bars->kempty[i], 1);
-      mbar_init(&bars->vempty[i], 1);
+      // With the fused append a tile's slots are also read by the cache writers.
+      mbar_init(&bars->kempty[i], p.append ? 2 : 1);
+      mbar_init(&bars->vempty[i], p.append ? 2 : 1);
       mbar_init(&bars->q_full[i], 1);
       mbar_init(&bars->q_empty[i], 1);
       mbar_init(&bars->s_full[i], 1);
@@ -252,6 +292,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&p.tm_kn);
       prefetch_tmap(&p.tm_kr);
       prefetch_tmap(&p.tm_v);
+      if (p.append) {
+        prefetch_tmap(&p.tm_kn_new);
+        prefetch_tmap(&p.tm_kr_new);
+        prefetch_tmap(&p.tm_v_new);
+      }
       const uint64_t pol_q = l2_policy_evict_first();
       // Sub-tile u goes to slot u % kSlots, whose previous occupant was sub-tile
       // u - kSlots of key tile (u - kSlots) / 5; that tile's K or V group must have been
@@ -294,7 +339,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = load_q(i, 0, w.r0, w.nt0, w.bh);
         q_units = i + 1;
         for (int j = 0; j < w.n && ok; ++j, ++g, u += kSubPerKv) {
-          const int jt = (j + w.js) * kBN;
+          // Key tile j + js; with the fused append the tiles past the cached prefix come from
+          // the new rows (row 0 of the new rows is key past_len = 128 n_pre).
+          const bool from_new = p.append && j + w.js >= p.n_pre;
+          const int jt = from_new ? (j + w.js - p.n_pre) * kBN : (j + w.js) * kBN;
+          const CUtensorMap* m_kn = from_new ? &p.tm_kn_new : &p.tm_kn;
+          const CUtensorMap* m_kr = from_new ? &p.tm_kr_new : &p.tm_kr;
+          const CUtensorMap* m_v = from_new ? &p.tm_v_new : &p.tm_v;
           // K(j): no-rope columns 0-63, 64-127 and the shared rotary tile, one barrier.
           uint64_t* kb = &bars->kfull[g & 1];
           for (int s = 0; s < 3 && ok; ++s) {
@@ -303,9 +354,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (s == 0) mbar_arrive_expect_tx(kb, 3 * kSub);
             uint8_t* dst = sRing + ((u + s) & (kSlots - 1)) * kSub;
             if (s < 2)
-              tma_load_3d_nohint(dst, &p.tm_kn, kb, 64 * s, jt, w.bh);
+              tma_load_3d_nohint(dst, m_kn, kb, 64 * s, jt, w.bh);
             else
-              tma_load_3d_nohint(dst, &p.tm_kr, kb, 0, jt, w.b);
+              tma_load_3d_nohint(dst, m_kr, kb, 0, jt, w.b);
           }
           if (!ok) break;
           // Q of the second tile after the first key tile: the first score MMA needs only
@@ -321,8 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = slot_free(u + 3) && slot_free(u + 4);
           if (!ok) break;
           mbar_arrive_expect_tx(vb, 2 * kSub);
-          tma_load_3d_nohint(sRing + min(sa, sb) * kSub, &p.tm_v, vb, 0, jt, w.bh);
-          tma_load_3d_nohint(sRing + max(sa, sb) * kSub, &p.tm_v, vb, 64, jt, w.bh);
+          tma_load_3d_nohint(sRing + min(sa, sb) * kSub, m_v, vb, 0, jt, w.bh);
+          tma_load_3d_nohint(sRing + max(sa, sb) * kSub, m_v, vb, 64, jt, w.bh);
         }
       }
       // Every load this thread issued must land before shared memory is released.  Each
@@ -336,6 +387,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         drain_wait(&bars->kfull[k & 1], (k >> 1) & 1);
         drain_wait(&bars->vfull[k & 1], (k >> 1) & 1);
       }
+    } else if ((warp == 2 || warp == 3) && lane == 0 && p.append) {
+      // ================= cache writers (fused append) =================
+      // warp 2: the key sub-tiles of every tile (kfull / kempty), warp 3: the value
+      // sub-tiles (vfull / vempty).  Each waits for a tile to land before it releases it,
+      // so a release of tile g + 2 implies both releases of tile g (its slots were refilled),
+      // and a store's source has been read before the release.  Owner of new key tile m:
+      // the unit whose query tile m holds it on its diagonal (query rows 128 m ...), which
+      // reads it whenever there is no kv_len; the rotary key (one per sequence) is written
+      // by head 0's owner.
+      const bool keys = warp == 2;
+      uint32_t u = 0, g = 0;
+      bool ok = true;
+      int kv_next = unit_kv(p, unit_index(p, 0));
+      for (int i = 0; ok; ++i) {
+        const int unit = unit_index(p, i);
+        if (unit < 0) break;
+        Unit w = unit_make(p, unit, kv_next);
+        unit_skip_hidden<kMasked>(p, w);
+        kv_next = unit_kv(p, unit_index(p, i + 1));
+        const int qt0 = w.r0 / kBM;  // the unit's first query tile
+        for (int j = 0; j < w.n && ok; ++j, ++g, u += kSubPerKv) {
+          const int kt = j + w.js;          // key tile
+          const int m = kt - p.n_pre;       // new-row tile, if >= 0
+          const bool own = m >= 0 && (m == qt0 || m == qt0 + 1) && m * kBM < p.Tq;
+          uint64_t* full = keys ? &bars->kfull[g & 1] : &bars->vfull[g & 1];
+          ok = mbar_wait(full, (g >> 1) & 1, p.status, abort_flag);
+          if (!ok) break;
+          if (own) {
+            fence_proxy_async_smem();
+            if (keys) {
+              for (int s = 0; s < 2; ++s)
+                tma_store_3d(&p.tm_kn_st, sRing + ((u + s) & (kSlots - 1)) * kSub, 64 * s,
+                             kt * kBN, w.bh);
+              if (w.bh % p.H == 0)
+                tma_store_3d(&p.tm_kr_st, sRing + ((u + 2) & (kSlots - 1)) * kSub, 0,
+                             kt * kBN, w.b);
+            } else {
+              const uint32_t sa = (u + 3) & (kSlots - 1), sb = (u + 4) & (kSlots - 1);
+              tma_store_3d(&p.tm_v_st, sRing + min(sa, sb) * kSub, 0, kt * kBN, w.bh);
+              tma_store_3d(&p.tm_v_st, sRing + max(sa, sb) * kSub, 64, kt * kBN, w.bh);
+            }
+            bulk_commit_group();
+            bulk_wait_read_all();
+          }
+          mbar_arrive(keys ? &bars->kempty[g & 1] : &bars->vempty[g & 1]);
+        }
+      }
+      bulk_wait_all();  // the cache rows are written before the kernel ends
     } else if (warp == 1) {
       // ================= MMA issuer =================
       // The whole warp runs this loop (waits, descriptor arithmetic: warp-uniform values);
@@ -707,17 +806,17 @@ bool encode_3d(EncodeTiledFn fn, CUtensorMap* m, const void* base, uint64_t inne
 // Host-side cache of encoded tensor maps, keyed by the five input pointers and the sizes:
 // a serving loop calls the same buffers over and over, and encoding costs microseconds.
 struct MapKey {
-  const void* ptr[5];
+  const void* ptr[8];  // q_nope, q_pe, k_nope, k_pe, v, then the new rows (append only)
   int B, H, Tq, Tk, kv_rows;
   bool operator==(const MapKey& o) const {
-    for (int i = 0; i < 5; ++i)
+    for (int i = 0; i < 8; ++i)
       if (ptr[i] != o.ptr[i]) return false;
     return B == o.B && H == o.H && Tq == o.Tq && Tk == o.Tk && kv_rows == o.kv_rows;
   }
 };
 struct MapEntry {
   MapKey key;
-  CUtensorMap maps[5];
+  CUtensorMap maps[11];
   bool valid;
 };
 constexpr int kMapCacheSize = 16;
@@ -726,16 +825,18 @@ MapEntry g_map_cache[kMapCacheSize];
 int g_map_next = 0;
 
 bool tensor_maps(const PrefillArgs& a, PrefillParams* p) {
-  const MapKey key = {{a.q_nope, a.q_pe, a.k_nope, a.k_pe, a.v}, a.B, a.H, a.Tq, a.Tk, a.kv_rows};
+  const MapKey key = {{a.q_nope, a.q_pe, a.k_nope, a.k_pe, a.v, a.new_k_nope, a.new_k_pe,
+                       a.new_v},
+                      a.B, a.H, a.Tq, a.Tk, a.kv_rows};
+  CUtensorMap* dst[11] = {&p->tm_qn,     &p->tm_qr,     &p->tm_kn,    &p->tm_kr,
+                          &p->tm_v,      &p->tm_kn_new, &p->tm_kr_new, &p->tm_v_new,
+                          &p->tm_kn_st,  &p->tm_kr_st,  &p->tm_v_st};
+  const int n_maps = a.new_k_nope ? 11 : 5;
   {
     std::lock_guard<std::mutex> lk(g_map_mu);
     for (const MapEntry& e : g_map_cache) {
       if (e.valid && e.key == key) {
-        p->tm_qn = e.maps[0];
-        p->tm_qr = e.maps[1];
-        p->tm_kn = e.maps[2];
-        p->tm_kr = e.maps[3];
-        p->tm_v = e.maps[4];
+        for (int k = 0; k < n_maps; ++k) *dst[k] = e.maps[k];
         return true;
       }
     }
@@ -749,15 +850,22 @@ bool tensor_maps(const PrefillArgs& a, PrefillParams* p) {
       !encode_3d(fn, &p->tm_kr, a.k_pe, 64, a.Tk, a.B, a.kv_rows) ||
       !encode_3d(fn, &p->tm_v, a.v, 128, a.Tk, BH, a.kv_rows))
     return false;
+  if (a.new_k_nope) {
+    // New rows [B,H,Tq,*] / [B,Tq,64]; the stores go to the caches' rows [0, Tk) (the
+    // maps clip a tile's rows past Tk).
+    if (!encode_3d(fn, &p->tm_kn_new, a.new_k_nope, 128, a.Tq, BH, a.Tq) ||
+        !encode_3d(fn, &p->tm_kr_new, a.new_k_pe, 64, a.Tq, a.B, a.Tq) ||
+        !encode_3d(fn, &p->tm_v_new, a.new_v, 128, a.Tq, BH, a.Tq) ||
+        !encode_3d(fn, &p->tm_kn_st, a.k_nope, 128, a.Tk, BH, a.kv_rows) ||
+        !encode_3d(fn, &p->tm_kr_st, a.k_pe, 64, a.Tk, a.B, a.kv_rows) ||
+        !encode_3d(fn, &p->tm_v_st, a.v, 128, a.Tk, BH, a.kv_rows))
+      return false;
+  }
   std::lock_guard<std::mutex> lk(g_map_mu);
   MapEntry& e = g_map_cache[g_map_next];
   g_map_next = (g_map_next + 1) % kMapCacheSize;
   e.key = key;
-  e.maps[0] = p->tm_qn;
-  e.maps[1] = p->tm_qr;
-  e.maps[2] = p->tm_kn;
-  e.maps[3] = p->tm_kr;
-  e.maps[4] = p->tm_v;
+  for (int k = 0; k < n_maps; ++k) e.maps[k] = *dst[k];
   e.valid = true;
   return true;
 }
@@ -832,7 +940,7 @@ bool encode_bf16_tiled(CUtensorMap* m, const void* base, int rank, const uint64_
 }
 
 cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
-  PrefillParams p;
+  PrefillParams p{};
   if (!tensor_maps(a, &p)) return cudaErrorInvalidValue;
   const uint64_t BH = (uint64_t)a.B * a.H;
   p.kv_len = a.kv_len;
@@ -845,6 +953,10 @@ cudaError_t launch_prefill(const PrefillArgs& a, cudaStream_t stream) {
   p.Tq = a.Tq;
   p.Tk = a.Tk;
   p.past_len = a.past_len;
+  p.append = a.new_k_nope != nullptr ? 1 : 0;
+  p.n_pre = a.past_len / kBN;
+  if (p.append && (a.past_len % kBN != 0 || a.kv_len != nullptr || a.key_bits != nullptr))
+    return cudaErrorInvalidValue;
   p.n_qb = (a.Tq + 2 * kBM - 1) / (2 * kBM);
   p.scale_log2 = a.scale_log2;
   const uint64_t units = BH * (uint64_t)p.n_qb;

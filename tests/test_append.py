@@ -66,6 +66,30 @@ def test_append_matches_oracle_and_writes_cache(B, H, Tq, past, T_cap, kv):
     _check_cache(inp, cache, past, Tq, T_cap)
 
 
+@pytest.mark.parametrize("B,H,Tq,past,T_cap", [
+    (2, 3, 130, 0, 300),      # empty cache: every key tile comes from the new rows
+    (2, 2, 300, 256, 700),    # two cached tiles, then new rows; ragged last tile
+    (1, 4, 129, 128, 257),    # capacity exactly Tk: the last tile's stores are clipped
+    (3, 2, 512, 384, 1024),   # several units own new tiles; B > 1 (one rotary row per b)
+])
+def test_prefill_append_fused_matches_oracle_and_writes_cache(B, H, Tq, past, T_cap):
+    """Prefill on a prefix of whole 128-key tiles with no kv_len: the attention kernel reads
+    the new rows from their own buffers and the unit holding each new tile on its diagonal
+    writes it into the caches."""
+    wl, inp, cache, new = _case(B, H, Tq, past, T_cap, None, seed=24)
+    d = to_device(inp)
+    out = binding.mla_attn_append_fwd(d["q_nope"], d["q_pe"], new["k_nope"],
+                                      new["k_pe_shared"], new["v"], cache["k_nope"],
+                                      cache["k_pe_shared"], cache["v"], None, past,
+                                      inp["softmax_scale"])
+    torch.cuda.synchronize()
+    assert_close(gpu_rows(out), oracle_for(inp), f"fused append B{B} H{H} Tq{Tq} past{past}")
+    _check_cache(inp, cache, past, Tq, T_cap)
+    # the same keys from one contiguous buffer give the same bits
+    d["kv_len"] = None
+    assert torch.equal(out.cpu(), run_gpu(d).cpu())
+
+
 def test_decode_append_equals_attention_on_the_filled_cache():
     wl, inp, cache, new = _case(4, 8, 1, 511, 640, None, seed=22)
     d = to_device(inp)

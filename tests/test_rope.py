@@ -50,11 +50,12 @@ def _case(B, H, Tq, past, T_cap, kv=None, seed=0, vs=1.0):
     return inp, cache, new
 
 
-def _run(inp, cache, new, table):
+def _run(inp, cache, new, table, kv_len=True):
+    """kv_len=False passes no kv_len (every sequence attends to all its keys)."""
+    kv = inp["kv_len"].cuda() if kv_len and inp["kv_len"] is not None else None
     out = binding.mla_attn_rope_append_fwd(
         inp["q_nope"].cuda(), inp["q_pe"].cuda(), new["k_nope"], new["k_pe_shared"], new["v"],
-        cache["k_nope"], cache["k_pe_shared"], cache["v"],
-        None if inp["kv_len"] is None else inp["kv_len"].cuda(), inp["past_len"],
+        cache["k_nope"], cache["k_pe_shared"], cache["v"], kv, inp["past_len"],
         inp["softmax_scale"], table)
     torch.cuda.synchronize()
     return out
@@ -117,6 +118,22 @@ def test_rope_append_matches_oracle_and_writes_cache(B, H, Tq, past, T_cap, kv, 
     _check_cache(inp, cache, c, T_cap)
 
 
+@pytest.mark.parametrize("B,H,Tq,past,T_cap,c", [
+    (2, 3, 130, 0, 300, RATIO),    # empty cache, ratio != 1
+    (1, 4, 200, 256, 600, PAGE),   # cached tiles, then rotated new rows
+    (2, 2, 129, 128, 257, PAGE),   # capacity exactly Tk
+])
+def test_rope_append_fused_prefill(B, H, Tq, past, T_cap, c):
+    """Prefill on a prefix of whole key tiles without kv_len: the rotary pass only rotates
+    (queries, and new rotary keys into the workspace); the attention kernel reads the new
+    rows and writes all three into the caches."""
+    inp, cache, new = _case(B, H, Tq, past, T_cap, None, seed=43)
+    table = binding.mla_rope_table(T_cap, _cfg(c))
+    out = _run(inp, cache, new, table, kv_len=False)
+    assert_close(gpu_rows(out), _oracle(inp, c), f"fused rope B{B} H{H} Tq{Tq} past{past}")
+    _check_cache(inp, cache, c, T_cap)
+
+
 def test_decode_steps_build_the_same_cache_as_one_prefill():
     B, H, N, T_cap = 2, 4, 40, 64
     inp, cache_p, new = _case(B, H, N, 0, T_cap, None, seed=42)
@@ -149,11 +166,19 @@ def test_long_prefill_with_rope_sampled():
     w = WORKLOADS["long_prefill"]
     inp, cache, new = _case(w.B, w.H, w.Tq, 0, w.Tq, None, seed=0, vs=w.value_scale)
     table = binding.mla_rope_table(w.Tq)
-    out = _run(inp, cache, new, table)
     rng = np.random.default_rng(3)
     qs = sorted({0, 1, 127, 128, 2047, 4095, *rng.integers(0, w.Tq, 8).tolist()})
     rows = [h * w.Tq + i for h in (0, 33, 63) for i in qs]
-    assert_close(gpu_rows(out, rows), _oracle(inp, PAGE, rows), "long_prefill rope sampled")
+    want = _oracle(inp, PAGE, rows)
+    # with kv_len (rotary pass copies, then attention) and without (the fused append, the
+    # bench's call): the same rows, and the fused call fills the cache completely
+    out = _run(inp, cache, new, table)
+    assert_close(gpu_rows(out, rows), want, "long_prefill rope sampled")
+    _, cache2, _ = _case(w.B, w.H, w.Tq, 0, w.Tq, None, seed=0, vs=w.value_scale)
+    out2 = _run(inp, cache2, new, table, kv_len=False)
+    assert_close(gpu_rows(out2, rows), want, "long_prefill rope fused, sampled")
+    for k in cache:
+        assert torch.equal(cache[k], cache2[k]), k
 
 
 def test_ragged_decode_with_rope_sampled():
