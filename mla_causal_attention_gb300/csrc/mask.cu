@@ -77,9 +77,7 @@ __global__ void __launch_bounds__(256) masked_rows_fixup_kernel(const FixupArgs 
     const size_t bh = (size_t)b * a.H + h;
     const uint16_t* vb = a.v + bh * a.kv_rows * 128 + col;
     float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-    for (int j = r0; j < a.Tk; j += 128) {
-      const uint4 w = *reinterpret_cast<const uint4*>(vb + (size_t)j * 128);
+    auto add = [&](const uint4 w) {
       s[0] += bf16lo_to_f32(w.x);
       s[1] += bf16hi_to_f32(w.x);
       s[2] += bf16lo_to_f32(w.y);
@@ -88,7 +86,19 @@ __global__ void __launch_bounds__(256) masked_rows_fixup_kernel(const FixupArgs 
       s[5] += bf16hi_to_f32(w.z);
       s[6] += bf16lo_to_f32(w.w);
       s[7] += bf16hi_to_f32(w.w);
+    };
+    // Eight independent 16-byte loads in flight per thread (the read of V is latency-bound:
+    // bytes in flight per SM set its rate), then the sums.
+    int j = r0;
+    for (; j + 7 * 128 < a.Tk; j += 8 * 128) {
+      uint4 w[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        w[k] = __ldcs(reinterpret_cast<const uint4*>(vb + (size_t)(j + k * 128) * 128));
+#pragma unroll
+      for (int k = 0; k < 8; ++k) add(w[k]);
     }
+    for (; j < a.Tk; j += 128) add(__ldcs(reinterpret_cast<const uint4*>(vb + (size_t)j * 128)));
     // Lanes of one column half differ in bits 1..4.
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
