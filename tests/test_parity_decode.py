@@ -65,6 +65,22 @@ def test_decode_calls_with_changing_plans_share_a_workspace():
         assert_close(gpu_rows(out), oracle_for(inp), f"decode sequence call {k}")
 
 
+def test_decode_long_context_every_row():
+    """One sequence with 131072 cached keys (4.3 GB of keys and values): the scheduler's
+    widest splits, every output row against the oracle."""
+    inp = make_inputs(wl(1, 64, 131071), seed=6)
+    out = run_gpu(to_device(inp))
+    assert_close(gpu_rows(out), oracle_for(inp), "decode Tk=131072")
+
+
+def test_decode_many_sequences_every_row():
+    """128 sequences x 64 heads with short ragged caches: 2048 head groups (13 waves of the
+    large configuration), one split each."""
+    inp = make_inputs(wl(128, 64, 47, (1, 48)), seed=7)
+    out = run_gpu(to_device(inp))
+    assert_close(gpu_rows(out), oracle_for(inp), "decode B=128 Tk<=48")
+
+
 def test_decode_single_key_is_exact():
     inp = make_inputs(wl(3, 8, 40, (1, 1)), seed=2)
     inp["kv_len"][:] = 1

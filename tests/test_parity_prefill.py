@@ -61,6 +61,22 @@ def test_chunked_prefill_full_size_every_row():
     assert_close(gpu_rows(out), oracle_for(inp), "chunked_prefill every row")
 
 
+def test_prefill_long_sequence_every_row():
+    """8192 new rows on 8192 cached ones (Tk = 16384, 64 key tiles per query tile at the
+    end), two heads: every output row against the oracle."""
+    inp = make_inputs(wl(1, 2, 8192, 8192), seed=11)
+    out = run_gpu(to_device(inp))
+    assert_close(gpu_rows(out), oracle_for(inp), "prefill Tq=8192 past=8192")
+
+
+def test_prefill_many_units_every_row():
+    """64 sequences x 64 heads x 300 rows: 8192 work units over the persistent grid, ragged
+    kv_len inside the causal range."""
+    inp = make_inputs(wl(64, 64, 300, 20, (100, 320)), seed=12)
+    out = run_gpu(to_device(inp))
+    assert_close(gpu_rows(out), oracle_for(inp), "prefill B64 H64 Tq300")
+
+
 def test_prefill_first_row_is_exact():
     inp = make_inputs(wl(2, 3, 200, 0), seed=7)
     out = run_gpu(to_device(inp)).cpu()
