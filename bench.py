@@ -817,7 +817,7 @@ def compact(res):
     """One short secondary entry from a measurement result."""
     rf = res.get("roofline") or {}
     c = {"v": _r(res.get("value")), "u": res.get("unit"), "ms": _r(res.get("ms_per_step")),
-         "frac": _r(rf.get("frac"), 3), "bound": rf.get("bound"), "peak": rf.get("peak")}
+         "frac": _r(rf.get("frac"), 3), "bound": rf.get("bound")}
     if rf.get("traffic"):
         c["traffic"] = rf["traffic"]
     clk = res.get("clocks") or {}
@@ -893,8 +893,10 @@ def main():
                 line[k] = res[k]
         line["step_ms_min"] = res["step_ms_min"]
         line["step_ms_max"] = res["step_ms_max"]
-        # Last in the line, one short object per workload: value, unit, ms per call,
-        # fraction of the measured peak, bound, median SM clock, the CPU oracle's rate.
+        # The measured peaks the secondary fractions are taken against, then, last in the
+        # line, one short object per workload: value, unit, ms per call, fraction of the
+        # measured peak of its bound, median SM clock, the CPU oracle's rate.
+        line["peaks"] = {"hbm": peak_for("hbm", False)[0], "tensor": peak_for("tensor", False)[0]}
         line["secondary"] = sec
         print(json.dumps(line, separators=(",", ":")))
     if world > 1:
