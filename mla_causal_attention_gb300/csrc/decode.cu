@@ -83,7 +83,9 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
 
 // KM: the 2D padding mask on keys is applied (p.key_mask); a separate instantiation so the
 // unmasked kernel carries none of its per-key work.
-template <int G, int T, int NST, int WPH, int MINB, bool KM>
+// ROPE: q_pe and the new key row arrive unrotated (p.rope_cs); a separate instantiation so
+// the other kernels carry none of its registers or per-pass work.
+template <int G, int T, int NST, int WPH, int MINB, bool KM, bool ROPE>
 __global__ void __launch_bounds__(DecCfg<G, T, NST, WPH>::kThreads, MINB)
     decode_splitkv_kernel(const DecodeArgs p) {
   using C = DecCfg<G, T, NST, WPH>;
@@ -93,6 +95,7 @@ __global__ void __launch_bounds__(DecCfg<G, T, NST, WPH>::kThreads, MINB)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + NST * C::kStageBytes + C::kMergeBytes);
   uint64_t* empty = full + NST;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + NST);
+  uint64_t* rot_done = empty + NST + 1;  // the new key row rotated (ROPE only, one phase)
 
   const int hg = blockIdx.x;
   const int split = blockIdx.y;
@@ -121,6 +124,7 @@ __global__ void __launch_bounds__(DecCfg<G, T, NST, WPH>::kThreads, MINB)
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], C::kConsumerWarps);
     }
+    if (ROPE) mbar_init(rot_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -183,11 +187,42 @@ __global__ void __launch_bounds__(DecCfg<G, T, NST, WPH>::kThreads, MINB)
   // this split the 8 lanes of a key read each 128-byte half-row of shared memory once,
   // so the 4 keys of a pass hit every bank exactly once per 16-byte load.
   float qn[16], qr[8];
+  // With the rotary step: the cos / sin of this lane's eight rotary columns at position
+  // Tk - 1 (the query's, and the new key's), columns 8 (l8 & 3) .. + 8 of either half.
+  // Loaded where they are used (L2-resident), so they are not live across the key loop.
+  constexpr bool rope = ROPE;
+  auto rope_cs = [&](float (&c)[8], float (&sn)[8], int slice) {
+    const float4* cs = reinterpret_cast<const float4*>(p.rope_cs + 8 * slice);
+    const float4* ss = reinterpret_cast<const float4*>(p.rope_cs + 32 + 8 * slice);
+    const float4 c0 = cs[0], c1 = cs[1], s0 = ss[0], s1 = ss[1];
+    c[0] = c0.x; c[1] = c0.y; c[2] = c0.z; c[3] = c0.w;
+    c[4] = c1.x; c[5] = c1.y; c[6] = c1.z; c[7] = c1.w;
+    sn[0] = s0.x; sn[1] = s0.y; sn[2] = s0.z; sn[3] = s0.w;
+    sn[4] = s1.x; sn[5] = s1.y; sn[6] = s1.z; sn[7] = s1.w;
+  };
   {
     const uint16_t* qsrc = p.q_nope + bh * 128 + l8 * 8;
     load8(qsrc, p.scale_log2, qn);
     load8(qsrc + 64, p.scale_log2, qn + 8);
-    load8(p.q_pe + bh * 64 + l8 * 8, p.scale_log2, qr);
+    if (rope) {
+      // The rotary pair of column d is d + 32: lanes l8 and l8 ^ 4 of a key group.
+      const uint4 own = *reinterpret_cast<const uint4*>(p.q_pe + bh * 64 + l8 * 8);
+      const uint4 other = make_uint4(__shfl_xor_sync(0xffffffffu, own.x, 4),
+                                     __shfl_xor_sync(0xffffffffu, own.y, 4),
+                                     __shfl_xor_sync(0xffffffffu, own.z, 4),
+                                     __shfl_xor_sync(0xffffffffu, own.w, 4));
+      float rc[8], rs[8];
+      rope_cs(rc, rs, l8 & 3);
+      const uint4 rot = rope_rotate8(own, other, rc, rs, l8 >= 4);
+      const uint32_t w[4] = {rot.x, rot.y, rot.z, rot.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        qr[2 * k] = bf16lo_to_f32(w[k]) * p.scale_log2;
+        qr[2 * k + 1] = bf16hi_to_f32(w[k]) * p.scale_log2;
+      }
+    } else {
+      load8(p.q_pe + bh * 64 + l8 * 8, p.scale_log2, qr);
+    }
   }
 
   // Fused cache append: split 0 of each head group writes the new key/value rows into the
@@ -198,9 +233,19 @@ __global__ void __launch_bounds__(DecCfg<G, T, NST, WPH>::kThreads, MINB)
         reinterpret_cast<const uint4*>(p.new_k_nope + bh * 128)[lane];
     reinterpret_cast<uint4*>(p.cache_v + row * 128)[lane] =
         reinterpret_cast<const uint4*>(p.new_v + bh * 128)[lane];
-    if (hg == 0 && g == 0 && lane < 8)
-      reinterpret_cast<uint4*>(p.cache_k_pe + ((size_t)b * p.kv_rows + p.Tk - 1) * 64)[lane] =
-          reinterpret_cast<const uint4*>(p.new_k_pe + (size_t)b * 64)[lane];
+    if (hg == 0 && g == 0 && lane < 8) {
+      uint4 kp = reinterpret_cast<const uint4*>(p.new_k_pe + (size_t)b * 64)[lane];
+      if (rope) {  // lanes 0..7 hold the row's eight column slices; pairs are lane ^ 4
+        const uint4 other = make_uint4(__shfl_xor_sync(0xffu, kp.x, 4),
+                                       __shfl_xor_sync(0xffu, kp.y, 4),
+                                       __shfl_xor_sync(0xffu, kp.z, 4),
+                                       __shfl_xor_sync(0xffu, kp.w, 4));
+        float rc[8], rs[8];
+        rope_cs(rc, rs, lane & 3);
+        kp = rope_rotate8(kp, other, rc, rs, lane >= 4);
+      }
+      reinterpret_cast<uint4*>(p.cache_k_pe + ((size_t)b * p.kv_rows + p.Tk - 1) * 64)[lane] = kp;
+    }
   }
 
   float m_run = -1e30f;  // finite sentinel: 2^(m_run - m_new) stays defined
@@ -223,11 +268,36 @@ __global__ void __launch_bounds__(DecCfg<G, T, NST, WPH>::kThreads, MINB)
     const int slot = it % NST;
     const int jt = j0 + it * T;
     const int nt = min(T, j1 - jt);
+    // With the rotary step, this stage's new-token row (key Tk - 1, taken from the new
+    // buffers) arrives unrotated: the lanes of that key rotate their slices in registers.
+    const bool rot_stage = rope && p.new_k_nope != nullptr && jt + nt == p.Tk;
     bool hidden[C::kPasses];
 #pragma unroll
     for (int ps = 0; ps < C::kPasses; ++ps) hidden[ps] = KM && mnext[ps] == 0;
     if (KM) load_mask(it + 1);
     if (!mbar_wait(&full[slot], (it / NST) & 1, p.status, abort_flag)) break;
+    if (rot_stage) {
+      // The stage's last row is the new key's rotary part, unrotated: lanes 0..7 of the first
+      // consumer warp rotate it in place (pairs are lane ^ 4) and signal an mbarrier that
+      // the other consumer warps wait on (bounded, like every wait).  One such stage per CTA.
+      if (warp == 0) {
+        if (lane < 8) {
+          uint4* row = reinterpret_cast<uint4*>(stages + slot * C::kStageBytes + (nt - 1) * 128);
+          const uint4 own = row[lane];
+          const uint4 other = make_uint4(__shfl_xor_sync(0xffu, own.x, 4),
+                                         __shfl_xor_sync(0xffu, own.y, 4),
+                                         __shfl_xor_sync(0xffu, own.z, 4),
+                                         __shfl_xor_sync(0xffu, own.w, 4));
+          float rc[8], rs[8];
+          rope_cs(rc, rs, lane & 3);
+          row[lane] = rope_rotate8(own, other, rc, rs, lane >= 4);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(rot_done);
+      } else if (!mbar_wait(rot_done, 0, p.status, abort_flag)) {
+        break;
+      }
+    }
     if (head_ok) {
       const uint8_t* st = stages + slot * C::kStageBytes;
       const uint8_t* kpe_s = st;
@@ -385,11 +455,11 @@ __global__ void __launch_bounds__(256) decode_combine_kernel(const DecodeArgs p)
   *reinterpret_cast<uint2*>(p.out + (size_t)w * 128 + lane * 4) = o;
 }
 
-template <int T, int MINB, bool KM>
+template <int T, int MINB, bool KM, bool ROPE>
 cudaError_t launch_split(const DecodeArgs& a, cudaStream_t stream) {
   constexpr int G = kDecHeadsPerCta, NST = 3, WPH = 2;
   using C = DecCfg<G, T, NST, WPH>;
-  auto kern = decode_splitkv_kernel<G, T, NST, WPH, MINB, KM>;
+  auto kern = decode_splitkv_kernel<G, T, NST, WPH, MINB, KM, ROPE>;
   static std::atomic<uint64_t> attr_done{0};  // bit per device: smem attribute set
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -412,12 +482,16 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   // Large problems: 32-key stages, 1 CTA per SM (213 KB of stages in flight per SM).
   // Small problems: 16-key stages, 2 CTAs per SM, so the grid fits in one wave.
   cudaError_t e;
+  if (a.key_mask && a.rope_cs) return cudaErrorInvalidValue;  // no such entry point
   if (a.key_mask)
-    e = a.small ? launch_split<kDecTokensPerStage / 2, 2, true>(a, stream)
-                : launch_split<kDecTokensPerStage, 1, true>(a, stream);
+    e = a.small ? launch_split<kDecTokensPerStage / 2, 2, true, false>(a, stream)
+                : launch_split<kDecTokensPerStage, 1, true, false>(a, stream);
+  else if (a.rope_cs)
+    e = a.small ? launch_split<kDecTokensPerStage / 2, 2, false, true>(a, stream)
+                : launch_split<kDecTokensPerStage, 1, false, true>(a, stream);
   else
-    e = a.small ? launch_split<kDecTokensPerStage / 2, 2, false>(a, stream)
-                : launch_split<kDecTokensPerStage, 1, false>(a, stream);
+    e = a.small ? launch_split<kDecTokensPerStage / 2, 2, false, false>(a, stream)
+                : launch_split<kDecTokensPerStage, 1, false, false>(a, stream);
   if (e != cudaSuccess || a.splits == 1) return e;
   // The combine pass is a programmatic dependent launch: its launch latency overlaps
   // the tail of the split kernel.

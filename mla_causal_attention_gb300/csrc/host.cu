@@ -219,6 +219,9 @@ struct AppendPtrs {
   uint16_t* cache_k_nope;
   uint16_t* cache_k_pe;
   uint16_t* cache_v;
+  // Decode only: q_pe and new_k_pe arrive unrotated and the decode kernel rotates them with
+  // this cos/sin table row (position Tk - 1); null: already rotated.
+  const float* rope_cs;
 };
 
 // Argument checks and launch shared by the attention entry points.  kv_rows is the row
@@ -281,6 +284,7 @@ mla_status attention_impl(const uint16_t* q_nope, const uint16_t* q_pe, const ui
       a.new_k_nope = app->new_k_nope; a.new_k_pe = app->new_k_pe; a.new_v = app->new_v;
       a.cache_k_nope = app->cache_k_nope; a.cache_k_pe = app->cache_k_pe;
       a.cache_v = app->cache_v;
+      a.rope_cs = app->rope_cs;
     }
     a.key_mask = key_mask;
     if (launch_decode(a, stream) != cudaSuccess) return MLA_ERR_CUDA;
@@ -351,7 +355,7 @@ mla_status mla_attn_append_fwd(const uint16_t* q_nope, const uint16_t* q_pe,
   const int Tk = past_len + Tq;
   if (Tq == 1) {
     // Decode: the append is fused into the attention kernel.
-    AppendPtrs app = {k_nope_new, k_pe_new, v_new, k_nope_cache, k_pe_cache, v_cache};
+    AppendPtrs app = {k_nope_new, k_pe_new, v_new, k_nope_cache, k_pe_cache, v_cache, nullptr};
     return attention_impl(q_nope, q_pe, k_nope_cache, k_pe_cache, v_cache, kv_len, B, H, Tq, Tk,
                           past_len, softmax_scale, out, workspace, workspace_bytes, cuda_stream,
                           nullptr, T_cap, &app);
@@ -359,7 +363,7 @@ mla_status mla_attn_append_fwd(const uint16_t* q_nope, const uint16_t* q_pe,
   if (prefill_can_fuse_append(past_len, kv_len, nullptr)) {
     // Prefill on a prefix of whole key tiles: the attention kernel reads the new rows where
     // they are and writes them into the caches itself.
-    AppendPtrs app = {k_nope_new, k_pe_new, v_new, k_nope_cache, k_pe_cache, v_cache};
+    AppendPtrs app = {k_nope_new, k_pe_new, v_new, k_nope_cache, k_pe_cache, v_cache, nullptr};
     return attention_impl(q_nope, q_pe, k_nope_cache, k_pe_cache, v_cache, kv_len, B, H, Tq, Tk,
                           past_len, softmax_scale, out, workspace, workspace_bytes, cuda_stream,
                           nullptr, T_cap, &app);
@@ -438,11 +442,20 @@ mla_status mla_attn_rope_append_fwd(const uint16_t* q_nope, const uint16_t* q_pe
   uint16_t* q_pe_rot = reinterpret_cast<uint16_t*>(rot);
   uint16_t* k_pe_rot = reinterpret_cast<uint16_t*>(rot + q_rot_bytes(B, H, Tq));
 
-  // Every check of the attention call runs before anything is enqueued.  Decode, and a
-  // prefill on a prefix of whole key tiles without kv_len, append inside the attention
+  if (Tq == 1) {
+    // Decode: one kernel rotates the query's and the new key's rotary parts (row past_len of
+    // the table), appends the new rows and attends.
+    AppendPtrs dec = {k_nope_new, k_pe_new_raw, v_new, k_nope_cache, k_pe_cache, v_cache,
+                      rope_table + (size_t)past_len * 64};
+    return attention_impl(q_nope, q_pe_raw, k_nope_cache, k_pe_cache, v_cache, kv_len, B, H, Tq,
+                          Tk, past_len, softmax_scale, out, workspace, workspace_bytes,
+                          cuda_stream, nullptr, T_cap, &dec);
+  }
+  // Prefill: every check of the attention call runs before anything is enqueued.  On a
+  // prefix of whole key tiles without kv_len the append happens inside the attention
   // kernel (from the rotated keys in the workspace); other prefills copy first.
-  AppendPtrs app = {k_nope_new, k_pe_rot, v_new, k_nope_cache, k_pe_cache, v_cache};
-  const bool fuse = Tq == 1 || prefill_can_fuse_append(past_len, kv_len, nullptr);
+  AppendPtrs app = {k_nope_new, k_pe_rot, v_new, k_nope_cache, k_pe_cache, v_cache, nullptr};
+  const bool fuse = prefill_can_fuse_append(past_len, kv_len, nullptr);
   const AppendPtrs* fused = fuse ? &app : nullptr;
   mla_status st = attention_impl(q_nope, q_pe_rot, k_nope_cache, k_pe_cache, v_cache, kv_len, B,
                                  H, Tq, Tk, past_len, softmax_scale, out, workspace,

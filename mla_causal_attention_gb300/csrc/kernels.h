@@ -40,6 +40,10 @@ struct DecodeArgs {
   uint16_t* cache_v;
   // Optional 2D padding mask [B][Tk] (0 = key hidden); null otherwise.
   const uint8_t* key_mask;
+  // Optional rotary step (with the fused append only): q_pe and new_k_pe arrive unrotated
+  // and are rotated at position Tk - 1 with this row of the cos/sin table (64 floats: cos of
+  // the 32 angles, then sin); null otherwise.
+  const float* rope_cs;
 };
 
 // Decode kernel configuration (shared with the scheduler).

@@ -226,4 +226,31 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// ---- rotary embedding (rotate-half form on the 64 rotary columns) ----------------------
+// y[d] = x[d] cos_d - x[d+32] sin_d,  y[d+32] = x[d+32] cos_d + x[d] sin_d  (d < 32), in
+// fp32, rounded once to bf16.  Eight columns at a time: `own` holds columns [c, c+8) of one
+// row and `other` the columns 32 away; `upper` says whether `own` is the half at 32..63.
+// cos_d / sin_d for the eight d of this slice.
+__device__ __forceinline__ uint4 rope_rotate8(const uint4 own, const uint4 other,
+                                              const float* cs_cos, const float* cs_sin,
+                                              bool upper) {
+  const uint32_t ow[4] = {own.x, own.y, own.z, own.w};
+  const uint32_t ot[4] = {other.x, other.y, other.z, other.w};
+  uint32_t r[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float y[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float xo = h ? bf16hi_to_f32(ow[k]) : bf16lo_to_f32(ow[k]);
+      const float xt = h ? bf16hi_to_f32(ot[k]) : bf16lo_to_f32(ot[k]);
+      const float c = cs_cos[2 * k + h], sn = cs_sin[2 * k + h];
+      // x1 = x[d], x2 = x[d+32]: lower half y = x1 c - x2 s, upper half y = x2 c + x1 s
+      y[h] = upper ? fmaf(xo, c, xt * sn) : fmaf(xo, c, -xt * sn);
+    }
+    r[k] = pack_bf16x2(y[0], y[1]);
+  }
+  return make_uint4(r[0], r[1], r[2], r[3]);
+}
+
 }  // namespace mla
