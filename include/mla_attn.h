@@ -143,9 +143,13 @@ MLA_API mla_status mla_attn_fwd_ex(const uint16_t* q_nope, const uint16_t* q_pe,
  * other arguments are those of mla_attn_fwd (kv_len, when given, still hides keys >=
  * kv_len[b]; the new rows are written at past_len regardless).  With Tq == 1 the append
  * is fused into the decode kernel (the stage holding the new row reads it from the new
- * buffers; one CTA per head group writes it to the cache); with Tq > 1 a copy kernel
- * appends the rows before the attention kernel runs.  Errors as for mla_attn_fwd;
- * MLA_ERR_SHAPE also when past_len + Tq > T_cap.
+ * buffers; one CTA per head group writes it to the cache).  With Tq > 1, past_len a
+ * multiple of 128 and kv_len NULL it is fused into the prefill kernel: key tiles past the
+ * cached prefix are read from the new buffers, and the work unit holding each such tile on
+ * its causal diagonal writes it into the caches (every new row is then read by its owner).
+ * Other prefills run a copy kernel that appends the rows before the attention kernel.  The
+ * output is the same either way.  Errors as for mla_attn_fwd; MLA_ERR_SHAPE also when
+ * past_len + Tq > T_cap.
  */
 MLA_API mla_status mla_attn_append_fwd(const uint16_t* q_nope, const uint16_t* q_pe,
                                        const uint16_t* k_nope_new, const uint16_t* k_pe_new,
@@ -297,11 +301,13 @@ MLA_API size_t mla_attn_rope_workspace_bytes(int B, int H, int Tq, int Tk);
  * stored rotated and are not rotated again); the rotated queries are kept in the
  * workspace (at least mla_attn_rope_workspace_bytes(B, H, Tq, past_len + Tq) bytes, zeroed
  * once like mla_attn_fwd's).  Rotated values are rounded to bf16, the type of the cache.
- * With Tq == 1 one small kernel rotates the query and the new rotary key into the
- * workspace and the decode kernel appends the new rows to the cache; with Tq > 1 one
- * kernel rotates the query, rotates and appends the rotary keys and appends the no-rope key
- * and value rows, then the prefill kernel runs.  All host checks run before anything is
- * enqueued.
+ * With Tq == 1 the decode kernel itself rotates the query and the new rotary key (one
+ * launch besides the split merge) and appends the new rows.  With Tq > 1 a rotation kernel
+ * runs first: for a prefill that fuses the append (past_len a multiple of 128, kv_len
+ * NULL; see mla_attn_append_fwd) it only rotates the queries and the new rotary keys into
+ * the workspace and the prefill kernel appends all three new rows; otherwise it also writes
+ * the rotated keys and the no-rope key and value rows into the caches before the prefill
+ * kernel runs.  All host checks run before anything is enqueued.
  */
 MLA_API mla_status mla_attn_rope_append_fwd(const uint16_t* q_nope, const uint16_t* q_pe_raw,
                                             const uint16_t* k_nope_new,
