@@ -84,16 +84,15 @@ def test_rows_with_no_visible_key_are_value_means():
         np.testing.assert_allclose(out[1, :, i], mean, rtol=0, atol=1e-2)
 
 
-def test_long_prefill_left_padded_sampled():
+def test_long_prefill_left_padded_every_row():
+    """The long prefill (8 heads) with its first 700 keys hidden: rows 0..699 see no key
+    (value means), every row against the oracle."""
     w = WORKLOADS["long_prefill"].with_(H=8)
     inp = make_inputs(w, seed=0)
     mask = np.ones((1, w.Tk), dtype=np.uint8)
     mask[0, :700] = 0
     out = _run(inp, mask)
-    rng = np.random.default_rng(5)
-    qs = sorted({0, 1, 699, 700, 701, 1023, 2048, 4095, *rng.integers(0, w.Tq, 8).tolist()})
-    rows = [h * w.Tq + i for h in (0, 7) for i in qs]
-    assert_close(gpu_rows(out, rows), _oracle(inp, mask, rows), "long_prefill left pad 700")
+    assert_close(gpu_rows(out), _oracle(inp, mask), "long_prefill left pad 700, every row")
 
 
 @pytest.mark.parametrize("B,H,Tq,past,pads", [
