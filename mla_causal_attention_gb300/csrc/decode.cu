@@ -353,7 +353,17 @@ __global__ void __launch_bounds__(DecCfg<G, T, NST, WPH>::kThreads, MINB)
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[slot]);
+#ifdef MLA_TEST_DROP_SLOT_RELEASE
+    // Test build only: the first consumer warp of CTA (0, 0, 0) withholds its release of the
+    // first stage's slot.  The producer's bounded wait for that slot then gives up, which
+    // exercises the timeout report and the CTA's unwinding (copies drained, no partial
+    // written).  The arrival carries no transaction bytes.
+    const bool withhold = blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && warp == 0 &&
+                          it == 0;
+#else
+    constexpr bool withhold = false;
+#endif
+    if (lane == 0 && !withhold) mbar_arrive(&empty[slot]);
   }
 
   // Merge the WPH warps of each head through shared memory.

@@ -202,7 +202,16 @@ __global__ void __launch_bounds__(256, 1) oproj_kernel(const __grid_constant__ O
             tc::mma_ss(acc, dhi | (uint64_t)(a_lo + koff), dhi | (uint64_t)(b_lo + koff),
                        kIdesc, (kb | kk) != 0 ? 1u : 0u);
           }
-          tc::commit(&bars->empty[s]);
+#ifdef MLA_TEST_DROP_STAGE_RELEASE
+          // Test build only: CTA 0 skips the release of its first stage.  The producers'
+          // bounded waits for that stage then give up, which exercises the timeout report
+          // and the unwinding (the MMAs in flight are still covered by the final commit
+          // that precedes the release of tensor memory).
+          const bool withhold = blockIdx.x == 0 && g == 0;
+#else
+          constexpr bool withhold = false;
+#endif
+          if (!withhold) tc::commit(&bars->empty[s]);
           if (kb == KB - 1) tc::commit(&bars->acc_full[ab]);
         }
         __syncwarp();

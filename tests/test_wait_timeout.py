@@ -1,17 +1,25 @@
-"""The bounded-wait path of the prefill kernel, exercised without any GPU fault.
+"""The bounded-wait paths of the kernels, exercised without any GPU fault.
 
 Every wait inside the kernels is bounded: past its limit it records MLA_ERR_TIMEOUT in the
 status word, raises a CTA-wide abort flag, waits (again bounded) for the CTA's own copies
-and MMAs in flight, releases tensor memory and returns.  A test build of the library
-(prefill.cu compiled with MLA_TEST_DROP_P_READY and a 2 ms wait limit; the library proper
-never sets either) has one softmax warp of CTA 0 withhold one P-ready arrival, a plain
-mbarrier arrive that starts no copy and carries no transaction bytes.  The MMA warp's wait
-for it runs out.  The test checks that the call returns within a bounded time with the
-status word set to MLA_ERR_TIMEOUT, and that the real library on the same GPU afterwards
-runs clean and matches the oracle.
+and MMAs in flight, releases tensor memory and returns.  Test builds of the library (one
+source compiled with a test-only define and a 2 ms wait limit; the library proper never
+sets either) each withhold one plain release that starts no copy and carries no transaction
+bytes:
+  - prefill.cu, MLA_TEST_DROP_P_READY: one softmax warp of CTA 0 withholds one P-ready
+    arrival, and the MMA warp's wait for it runs out;
+  - decode.cu, MLA_TEST_DROP_SLOT_RELEASE: one consumer warp of the first CTA withholds its
+    release of the first stage's slot, and the producer's wait to refill it runs out;
+  - oproj.cu, MLA_TEST_DROP_STAGE_RELEASE: the MMA warp of CTA 0 skips the commit that
+    releases its first stage, and the producers' waits to refill it run out.
+Each test checks that the call returns within a bounded time with the status word set to
+MLA_ERR_TIMEOUT, and that the real library on the same GPU afterwards runs clean and matches
+the oracle.
 """
 import ctypes
 import time
+
+import numpy as np
 
 import pytest
 import torch
@@ -21,19 +29,25 @@ from mla_causal_attention_gb300.build import build_test_variant
 from mla_causal_attention_gb300.inputs import make_inputs
 from mla_causal_attention_gb300.workloads import Workload, softmax_scale_192
 from gpu_helpers import assert_close, gpu_rows, oracle_for, run_gpu, to_device
+from oracle import oracle_oproj_rows
 
 pytestmark = pytest.mark.gpu
 
 
-def _timeout_library():
-    path = build_test_variant("wait_timeout", "prefill.cu",
-                              ["-DMLA_WAIT_LIMIT_NS=2000000ull", "-DMLA_TEST_DROP_P_READY=1"])
+def _timeout_library(name="wait_timeout", source="prefill.cu", drop="MLA_TEST_DROP_P_READY"):
+    path = build_test_variant(name, source, ["-DMLA_WAIT_LIMIT_NS=2000000ull", f"-D{drop}=1"])
     lib = ctypes.CDLL(path)
     p, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.mla_attn_fwd.restype = i
     lib.mla_attn_fwd.argtypes = [p, p, p, p, p, p, i, i, i, i, i, f, p, p, sz, p]
     lib.mla_attn_get_status.restype = i
     lib.mla_attn_get_status.argtypes = [p, p]
+    lib.mla_attn_workspace_bytes.restype = sz
+    lib.mla_attn_workspace_bytes.argtypes = [i, i, i, i]
+    lib.mla_oproj_workspace_bytes.restype = sz
+    lib.mla_oproj_workspace_bytes.argtypes = []
+    lib.mla_oproj_fwd.restype = i
+    lib.mla_oproj_fwd.argtypes = [p, p, i, i, i, i, p, p, sz, p]
     return lib
 
 
@@ -68,3 +82,69 @@ def test_prefill_wait_gives_up_reports_timeout_and_device_stays_usable():
     got = run_gpu(d)
     assert binding.mla_attn_get_status(device=torch.device("cuda")) == 0
     assert_close(gpu_rows(got), oracle_for(inp), "prefill after a timed-out launch")
+
+
+def test_decode_wait_gives_up_reports_timeout_and_device_stays_usable():
+    # The page's decode shape: 64 heads over 1001 cached keys, 64-key splits of four 16-key
+    # stages on a three-slot ring, so the producer of the first CTA waits to refill slot 0.
+    w = Workload("timeout_decode", 1, 64, 1, 1000, 1.0, None, softmax_scale_192())
+    inp = make_inputs(w, seed=32)
+    d = to_device(inp)
+    assert binding.decode_plan(1, 64, 1001) == (64, 16)
+    lib = _timeout_library("wait_timeout_decode", "decode.cu", "MLA_TEST_DROP_SLOT_RELEASE")
+    ws = torch.zeros(lib.mla_attn_workspace_bytes(1, 64, 1, 1001), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.zeros((1, 64, 1, 128), dtype=torch.bfloat16, device="cuda")
+    P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    rc = lib.mla_attn_fwd(P(d["q_nope"]), P(d["q_pe"]), P(d["k_nope"]), P(d["k_pe_shared"]),
+                          P(d["v"]), P(d["kv_len"]), 1, 64, 1, 1001, 1000,
+                          ctypes.c_float(d["softmax_scale"]), P(out), P(ws),
+                          ctypes.c_size_t(ws.numel()), stream)
+    assert rc == 0
+    st = lib.mla_attn_get_status(P(ws), stream)
+    elapsed = time.perf_counter() - t0
+    assert st == binding.MlaStatus.ERR_TIMEOUT, f"status {st}"
+    assert elapsed < 5.0, f"the aborted launch took {elapsed:.2f} s"
+    assert lib.mla_attn_get_status(P(ws), stream) == 0
+    torch.cuda.synchronize()
+
+    got = run_gpu(d)
+    assert binding.mla_attn_get_status(device=torch.device("cuda")) == 0
+    assert_close(gpu_rows(got), oracle_for(inp), "decode after a timed-out launch")
+
+
+def test_oproj_wait_gives_up_reports_timeout_and_device_stays_usable():
+    # The decode-width projection: 64 rows x 8192 -> 7168, one 48-column tile per CTA over
+    # 128 k-blocks on a ten-stage ring, so the producers of CTA 0 wait to refill stage 0.
+    B, H, T, N = 64, 64, 1, 7168
+    g = torch.Generator().manual_seed(33)
+    attn = torch.randn((B, H, T, 128), generator=g).to(torch.bfloat16)
+    w = (torch.randn((N, H * 128), generator=g) * (H * 128) ** -0.5).to(torch.bfloat16)
+    attn_d, w_d = attn.cuda(), w.cuda()
+    lib = _timeout_library("wait_timeout_oproj", "oproj.cu", "MLA_TEST_DROP_STAGE_RELEASE")
+    nb = lib.mla_oproj_workspace_bytes()
+    ws = torch.zeros(nb, dtype=torch.uint8, device="cuda")
+    y = torch.zeros((B, T, N), dtype=torch.bfloat16, device="cuda")
+    P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    rc = lib.mla_oproj_fwd(P(attn_d), P(w_d), B, H, T, N, P(y), P(ws), ctypes.c_size_t(nb),
+                           stream)
+    assert rc == 0
+    st = lib.mla_attn_get_status(P(ws), stream)
+    elapsed = time.perf_counter() - t0
+    assert st == binding.MlaStatus.ERR_TIMEOUT, f"status {st}"
+    assert elapsed < 5.0, f"the aborted launch took {elapsed:.2f} s"
+    assert lib.mla_attn_get_status(P(ws), stream) == 0
+    torch.cuda.synchronize()
+
+    got = binding.mla_oproj_fwd(attn_d, w_d)
+    torch.cuda.synchronize()
+    rows = np.arange(0, B * T, 7)
+    want = oracle_oproj_rows(attn, w, rows=rows)
+    assert_close(got.float().cpu().numpy().reshape(B * T, N)[rows].astype(np.float64), want,
+                 "o_proj after a timed-out launch")
