@@ -413,7 +413,15 @@ __global__ void __launch_bounds__(kLThreads, 1)
               const uint64_t bdesc = dhi_p | (uint64_t)(p_lo + kk * (2048 >> 4));
               tc::mma_ss(o_tmem + 64 * q, adesc, bdesc, kIdPV, (j > 0 || kk > 0) ? 1u : 0u);
             }
-            tc::commit(&bars->empty[2 * q]);
+#ifdef MLA_TEST_DROP_SLOT_RELEASE
+            // Test build only: CTA 0 skips the release of slot 0 after its first tile.  The
+            // producer's bounded wait to refill it then gives up, which exercises the timeout
+            // report and the unwinding (the final commit still covers every MMA in flight).
+            const bool withhold = blockIdx.x == 0 && g == 0 && q == 0;
+#else
+            constexpr bool withhold = false;
+#endif
+            if (!withhold) tc::commit(&bars->empty[2 * q]);
             tc::commit(&bars->empty[2 * q + 1]);
           }
 #pragma unroll

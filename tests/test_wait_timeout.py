@@ -11,7 +11,10 @@ bytes:
   - decode.cu, MLA_TEST_DROP_SLOT_RELEASE: one consumer warp of the first CTA withholds its
     release of the first stage's slot, and the producer's wait to refill it runs out;
   - oproj.cu, MLA_TEST_DROP_STAGE_RELEASE: the MMA warp of CTA 0 skips the commit that
-    releases its first stage, and the producers' waits to refill it run out.
+    releases its first stage, and the producers' waits to refill it run out;
+  - latent.cu, MLA_TEST_DROP_SLOT_RELEASE: the MMA warp of CTA 0 skips the commit that
+    releases latent slot 0 after its first tile, and the producer's wait to refill it runs
+    out.
 Each test checks that the call returns within a bounded time with the status word set to
 MLA_ERR_TIMEOUT, and that the real library on the same GPU afterwards runs clean and matches
 the oracle.
@@ -29,7 +32,7 @@ from mla_causal_attention_gb300.build import build_test_variant
 from mla_causal_attention_gb300.inputs import make_inputs
 from mla_causal_attention_gb300.workloads import Workload, softmax_scale_192
 from gpu_helpers import assert_close, gpu_rows, oracle_for, run_gpu, to_device
-from oracle import oracle_oproj_rows
+from oracle import oracle_latent_rows, oracle_oproj_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -48,6 +51,10 @@ def _timeout_library(name="wait_timeout", source="prefill.cu", drop="MLA_TEST_DR
     lib.mla_oproj_workspace_bytes.argtypes = []
     lib.mla_oproj_fwd.restype = i
     lib.mla_oproj_fwd.argtypes = [p, p, i, i, i, i, p, p, sz, p]
+    lib.mla_latent_workspace_bytes.restype = sz
+    lib.mla_latent_workspace_bytes.argtypes = [i, i, i]
+    lib.mla_latent_decode_fwd.restype = i
+    lib.mla_latent_decode_fwd.argtypes = [p, p, p, p, p, p, i, i, i, f, p, p, sz, p]
     return lib
 
 
@@ -148,3 +155,43 @@ def test_oproj_wait_gives_up_reports_timeout_and_device_stays_usable():
     want = oracle_oproj_rows(attn, w, rows=rows)
     assert_close(got.float().cpu().numpy().reshape(B * T, N)[rows].astype(np.float64), want,
                  "o_proj after a timed-out launch")
+
+
+def test_latent_wait_gives_up_reports_timeout_and_device_stays_usable():
+    # 8 sequences of 8192 latent rows: 512 key tiles over the CTAs, several per CTA, so the
+    # producer of CTA 0 waits to refill slot 0 for its second tile.
+    B, H, Tk = 8, 64, 8192
+    g = torch.Generator("cpu").manual_seed(34)
+    mk = lambda *s: torch.randn(*s, generator=g).to(torch.bfloat16)  # noqa: E731
+    h = dict(q_nope=mk(B, H, 128), q_pe=mk(B, H, 64), c_kv=mk(B, Tk, 512), k_pe=mk(B, Tk, 64),
+             w_kvb=(torch.randn(H * 256, 512, generator=g) / 512 ** 0.5).to(torch.bfloat16))
+    c = {k: v.cuda() for k, v in h.items()}
+    lib = _timeout_library("wait_timeout_latent", "latent.cu", "MLA_TEST_DROP_SLOT_RELEASE")
+    nb = lib.mla_latent_workspace_bytes(B, H, Tk)
+    ws = torch.zeros(nb, dtype=torch.uint8, device="cuda")
+    out = torch.zeros((B, H, 128), dtype=torch.bfloat16, device="cuda")
+    P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    scale = softmax_scale_192()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    rc = lib.mla_latent_decode_fwd(P(c["q_nope"]), P(c["q_pe"]), P(c["c_kv"]), P(c["k_pe"]),
+                                   P(c["w_kvb"]), None, B, H, Tk, ctypes.c_float(scale),
+                                   P(out), P(ws), ctypes.c_size_t(nb), stream)
+    assert rc == 0
+    st = lib.mla_attn_get_status(P(ws), stream)
+    elapsed = time.perf_counter() - t0
+    assert st == binding.MlaStatus.ERR_TIMEOUT, f"status {st}"
+    assert elapsed < 5.0, f"the aborted launch took {elapsed:.2f} s"
+    assert lib.mla_attn_get_status(P(ws), stream) == 0
+    torch.cuda.synchronize()
+
+    got = binding.mla_latent_decode_fwd(c["q_nope"], c["q_pe"], c["c_kv"], c["k_pe"],
+                                        c["w_kvb"], None, scale)
+    torch.cuda.synchronize()
+    assert binding.mla_attn_get_status(device=got.device) == 0
+    rows = np.arange(0, B * H, 5)
+    want = oracle_latent_rows(h["q_nope"][:, :, None], h["q_pe"][:, :, None], h["c_kv"],
+                              h["k_pe"], h["w_kvb"], None, Tk - 1, scale, rows=rows)
+    assert_close(got.float().cpu().numpy().reshape(-1, 128)[rows], want,
+                 "latent decode after a timed-out launch")
