@@ -728,9 +728,26 @@ def measure_e2e(wl, host, d, out, ws, stream, m, args, world):
     if not torch.equal(outs_host[last], out.cpu()):
         raise RuntimeError("e2e: the streamed output differs from the device-resident call")
     ms = max_over_ranks(e0.elapsed_time(e1) / steps, world, dev)
+
+    # The host link's own rates in this run, for reading the figure: one step's inputs in,
+    # then its output back, each copied alone.
+    def timed(fn):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    h2d_ms = min(timed(lambda: [sets[1][k].copy_(host[k], non_blocking=True) for k in keys])
+                 for _ in range(3))
+    d2h_ms = min(timed(lambda: outs_host[0].copy_(outs[0], non_blocking=True)) for _ in range(3))
     return {"value": whole_job_rate(m["work"], world, ms, m["scale"]), "unit": m["unit"],
             "ms_per_step": ms, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "steps": steps, "pipelined": True}
+            "steps": steps, "pipelined": True,
+            "link_gbs": {"h2d": round(h2d / (h2d_ms * 1e-3) / 1e9, 1),
+                         "d2h": round(d2h / (d2h_ms * 1e-3) / 1e9, 1)}}
 
 
 # ---------------------------------------------------------------------------------------
