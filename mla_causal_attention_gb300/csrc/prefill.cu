@@ -117,13 +117,15 @@ __device__ __forceinline__ void setmaxnreg_inc_softmax() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 208;" ::: "memory");
 }
 
-// Keeps the compiler from using tcgen05.ld destinations before tcgen05.wait::ld.
-__device__ __forceinline__ void pin32(uint32_t (&r)[32]) {
+// Keep the compiler from using tcgen05.ld destinations before tcgen05.wait::ld.
+template <int N>
+__device__ __forceinline__ void pin(uint32_t (&r)[N]) {
 #pragma unroll
-  for (int i = 0; i < 32; i += 8)
+  for (int i = 0; i < N; i += 8)
     asm volatile("" : "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]),
                  "+r"(r[i + 4]), "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7]));
 }
+__device__ __forceinline__ void pin32(uint32_t (&r)[32]) { pin<32>(r); }
 
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_u32(bar);
@@ -644,15 +646,18 @@ __global__ void __launch_bounds__(kThreads, 1)
               m = m_tile;
               l *= alpha;
             }
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              uint32_t o[32];
-              tc::tmem_ld32(o_tmem + c * 32, o);
+            // 16 columns at a time in a loop that is not unrolled: this rare branch runs
+            // while the tile's 128 scores are live, and wider or unrolled chunks made the
+            // softmax spill registers (3% on the long prefill).
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {
+              uint32_t o[16];
+              tc::tmem_ld16(o_tmem + c * 16, o);
               tc::tmem_wait_ld();
-              pin32(o);
+              pin<16>(o);
 #pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-              tc::tmem_st32(o_tmem + c * 32, o);
+              for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+              tc::tmem_st16(o_tmem + c * 16, o);
             }
           }
         }

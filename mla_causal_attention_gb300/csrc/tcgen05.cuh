@@ -136,6 +136,13 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       MLA_W8(0), MLA_W8(8), MLA_W8(16), MLA_W8(24)
       : "memory");
 }
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      MLA_W8(0), MLA_W8(8)
+      : "memory");
+}
 #undef MLA_W8
 
 __device__ __forceinline__ void tmem_wait_ld() {
