@@ -120,18 +120,17 @@ bool rope_config_ok(const mla_rope_config& c) {
 
 }  // namespace
 
-// Keys per split for the decode path.  When there are at least as many (sequence, head
-// group) units as SMs, the large configuration (32-key stages, 1 CTA per SM) takes the
-// largest power-of-two multiple of 64 keys (at most 1024) that still leaves two full
-// waves.  Smaller problems use the small configuration (16-key stages, 2 CTAs per SM) and
-// split the keys so that the whole grid is about one wave of 2 CTAs per SM.
+// Keys per split for the decode path (the kernel runs 2 CTAs per SM).  When there are at
+// least as many (sequence, head group) units as SMs, take the largest power-of-two multiple
+// of 64 keys (at most 1024) that still leaves two full waves of one CTA per SM.  Fewer
+// units split the keys so that the whole grid is about one wave of 2 CTAs per SM.
 DecodePlan plan_decode(int B, int H, int Tk, int sms, int forced_chunk) {
   const int64_t groups = (int64_t)B * ((H + kDecHeadsPerCta - 1) / kDecHeadsPerCta);
   DecodePlan pl;
-  pl.small = groups < (int64_t)sms ? 1 : 0;
+  const bool few = groups < (int64_t)sms;
   if (forced_chunk > 0) {
     pl.chunk = forced_chunk;
-  } else if (!pl.small) {
+  } else if (!few) {
     int c = kDecMinChunk;
     while (c < 1024) {
       const int64_t next = groups * ((Tk + 2 * c - 1) / (2 * c));
@@ -277,7 +276,7 @@ mla_status attention_impl(const uint16_t* q_nope, const uint16_t* q_pe, const ui
     uint8_t* part = static_cast<uint8_t*>(workspace) + kStatusBytes;
     a.part_ml = reinterpret_cast<float*>(part);
     a.part_acc = reinterpret_cast<float*>(part + decode_ml_bytes(B, H, splits));
-    a.B = B; a.H = H; a.Tk = Tk; a.chunk = chunk; a.splits = splits; a.small = pl.small;
+    a.B = B; a.H = H; a.Tk = Tk; a.chunk = chunk; a.splits = splits;
     a.scale_log2 = scale_log2;
     a.kv_rows = kv_rows;
     if (app) {

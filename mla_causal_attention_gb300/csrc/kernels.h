@@ -26,7 +26,6 @@ struct DecodeArgs {
   int B, H, Tk;
   int chunk;   // keys per split
   int splits;  // ceil(Tk / chunk)
-  int small;   // 1: 16-key stages, 2 CTAs per SM (problems smaller than one wave)
   float scale_log2;  // softmax_scale * log2(e)
   int kv_rows;       // rows per (b, h) of k_nope / v and per b of k_pe (>= Tk)
   // Optional fused cache append (all null otherwise): key row Tk-1 is taken from new_*
@@ -48,7 +47,7 @@ struct DecodeArgs {
 
 // Decode kernel configuration (shared with the scheduler).
 constexpr int kDecHeadsPerCta = 4;   // heads sharing one rotary-key tile
-constexpr int kDecTokensPerStage = 32;
+constexpr int kDecTokensPerStage = 16;
 constexpr int kDecMinChunk = 64;
 constexpr int kDecMaxChunk = 65536;
 
@@ -58,7 +57,6 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 struct DecodePlan {
   int chunk;
   int splits;
-  int small;
 };
 DecodePlan plan_decode(int B, int H, int Tk, int sms, int forced_chunk);
 

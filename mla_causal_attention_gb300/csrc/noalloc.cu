@@ -97,7 +97,6 @@ extern "C" mla_status mla_attn_decode_noalloc(const uint16_t* q_nope, const uint
   a.Tk = Tk;
   a.chunk = chunk;
   a.splits = splits;
-  a.small = pl.small;
   a.kv_rows = Tk;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   return launch_decode(a, static_cast<cudaStream_t>(cuda_stream)) == cudaSuccess ? MLA_OK
