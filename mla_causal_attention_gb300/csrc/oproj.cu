@@ -91,6 +91,27 @@ __device__ __forceinline__ OpTile op_tile(const OprojParams& p, int t, int bn) {
   return w;
 }
 
+// 2-D and 4-D tiled copies global -> shared with an L2 cache policy (createpolicy) for the
+// copied lines; the innermost coordinate times the element size must be a multiple of 16.
+__device__ __forceinline__ void tma_load_2d_policy(void* smem_dst, const void* tmap,
+                                                   uint64_t* bar, int c0, int c1,
+                                                   uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_4d_policy(void* smem_dst, const void* tmap,
+                                                   uint64_t* bar, int c0, int c1, int c2,
+                                                   int c3, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(smem_dst)),
+      "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 static_assert(sizeof(OpBars) <= 256, "barrier block");
 
 template <int BN>
@@ -137,6 +158,9 @@ __global__ void __launch_bounds__(256, 1) oproj_kernel(const __grid_constant__ O
     const int role = warp == 0 ? 0 : warp - 1;  // 0 = A, 1.. = weight box
     if (role <= C::kWProd) {
       prefetch_tmap(role == 0 ? (const void*)&p.tm_a : (const void*)&p.tm_w);
+      // The input is re-read by every column tile: keep it in L2.  Each weight byte is read
+      // once: let it go first.
+      const uint64_t pol = role == 0 ? l2_policy_evict_last() : l2_policy_evict_first();
       uint32_t g = 0;  // k-blocks posted over the run
       bool ok = true;
       for (int t = blockIdx.x; t < n_tiles && ok; t += G) {
@@ -152,12 +176,12 @@ __global__ void __launch_bounds__(256, 1) oproj_kernel(const __grid_constant__ O
           if (role == 0) {
             mbar_arrive_expect_tx(&bars->full[s], kOpASub);
             const int h = kb >> 1, d0 = (kb & 1) * kOpBK;
-            tma_load_4d(stage, &p.tm_a, &bars->full[s], d0, w.i0, h, w.b);
+            tma_load_4d_policy(stage, &p.tm_a, &bars->full[s], d0, w.i0, h, w.b, pol);
           } else {
             mbar_arrive_expect_tx(&bars->full[s], C::kBoxN * kOpBK * 2);
             const int r = (role - 1) * C::kBoxN;
-            tma_load_2d(stage + kOpASub + r * kOpBK * 2, &p.tm_w, &bars->full[s], kb * kOpBK,
-                        w.n0 + r);
+            tma_load_2d_policy(stage + kOpASub + r * kOpBK * 2, &p.tm_w, &bars->full[s],
+                               kb * kOpBK, w.n0 + r, pol);
           }
         }
       }
