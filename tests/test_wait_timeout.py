@@ -23,7 +23,6 @@ import ctypes
 import time
 
 import numpy as np
-
 import pytest
 import torch
 
